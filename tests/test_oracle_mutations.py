@@ -1,0 +1,43 @@
+"""Plants plausible mistakes in a temporary copy of the CPU oracle and checks that
+the oracle's pins (tests/test_oracle_pins.py) fail for each one.  The repository's
+oracle is never modified; each mutant is compiled and tested in a temp folder."""
+import os
+import shutil
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+MUTANTS = {
+    "nibble_swap": ("out32[j] = (float)(lo - 8) * d;", "out32[j] = (float)(hi - 8) * d;"),
+    "offset_7": ("out32[j + 16] = (float)(hi - 8) * d;", "out32[j + 16] = (float)(hi - 7) * d;"),
+    "qd_minus_8d": ("out32[j] = (float)(lo - 8) * d;", "out32[j] = (float)lo * d - 8.0f * d;"),
+    "scale_big_endian": ("uint16_t dbits = (uint16_t)(blk[0] | (blk[1] << 8));",
+                         "uint16_t dbits = (uint16_t)(blk[1] | (blk[0] << 8));"),
+    "subnormal_exp": ("v = ldexpf((float)frac, -24);", "v = ldexpf((float)frac, -25);"),
+    "ties_to_odd": ("fmod(fl, 2.0) == 1.0", "fmod(fl, 2.0) == 0.0"),
+    "max_last_index": ("if (fabsf(x[i]) > amax) {", "if (fabsf(x[i]) >= amax) {"),
+    "scale_sign": ("float d32 = x[im] / -8.0f;", "float d32 = x[im] / 8.0f;"),
+    "unrounded_scale": ("float t = x[i] / dd;", "float t = x[i] / (x[im] / -8.0f);"),
+    "truncating_round": ("float u = t + 8.5f;", "float u = t + 8.0f;"),
+    "no_clamp_15": ("if (fq > 15.0f) fq = 15.0f;", "if (fq > 16.0f) fq = 15.0f;"),
+    "fp32_accumulate": ("double y = 0.0, s = 0.0;", "float y = 0.0, s = 0.0;"),
+    "gather_no_status": ("rc = Q4O_ERR_ID_OUT_OF_RANGE;", "rc = Q4O_OK;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistake(tmp_path, name):
+    before, after = MUTANTS[name]
+    src = open(os.path.join(ROOT, "oracle", "q4_oracle.c")).read()
+    assert before in src, f"mutation site for {name} no longer exists"
+    for sub in ("oracle", "tests", "synth"):
+        shutil.copytree(os.path.join(ROOT, sub), tmp_path / sub,
+                        ignore=shutil.ignore_patterns("*.so", "__pycache__", "*.tmp*"))
+    (tmp_path / "oracle" / "q4_oracle.c").write_text(src.replace(before, after))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
+                        "tests/test_oracle_pins.py"], cwd=tmp_path, capture_output=True,
+                       text=True, timeout=600)
+    assert r.returncode != 0, f"mutant {name} passed every pin:\n{r.stdout[-2000:]}"
