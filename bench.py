@@ -1,0 +1,421 @@
+"""Benchmark of the GGUF Q4_0 linear layer on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Headline workload: the 26-layer decoder linear stack at batch-1 decode
+(hidden 3072, GQA 32Q/8KV, FFN 9216; Q4_0 weights N(0, 0.02^2) quantized on
+the device, activation N(0, 1) fp32).  A step is one decode token: 104
+dependent fused dequant-GEMV launches (per layer: [wq;wk;wv], wo, [w1;w3], w2)
+with programmatic dependent launch, replayed from CUDA graphs.  `value` is
+weight GB/s = Q4 bytes streamed per step x steps / device time.  The weights
+(1.70 GB) are ~13x the 126 MB L2, so every step reads them from HBM.
+
+The same line carries: the roofline of the GEMV kernel against the measured
+HBM copy bandwidth; `e2e` (per step: host->device copy of the token's input
+from pinned memory, the step, device->host copy of the layer-stack output);
+the prefill/encoder GEMM (32 layers x 4 linears of the 1280-wide encoder at
+3000 frames) in TFLOP/s against the measured bf16 peak; the batch-1 output
+head and embedding gather; and the CPU oracle timed on a bounded sample.
+
+--impl reference times the CPU oracle (plain C, fp64 sums) on the host cores,
+one decoder layer's [wq;wk;wv] product per step, same metric and unit.
+Under torchrun each rank runs an independent replica (no collective on the
+data path); timing is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "Q4_0 decode GEMV weight GB/s (% of HBM peak); prefill GEMM TFLOP/s (% peak)"
+WORKLOAD = ("decoder linear stack, 26 layers, batch-1 decode: per layer Q4_0 "
+            "wq 3072->4096, wk/wv 3072->1024, wo 4096->3072, w1/w3 3072->9216, w2 9216->3072")
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p["bf16_tflops_sustained"]), \
+            "measured"
+    except Exception:
+        return 6400.0, 1800.0, 1400.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except FileNotFoundError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def _barrier_max(value: float, world: int, torch):
+    if world == 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _oracle_sample(seconds: float = 12.0, mats=("qkv", "wo", "w13", "w2")):
+    """CPU oracle on one decoder layer (bounded): weight GB/s on all host cores."""
+    import numpy as np
+
+    import oracle
+    import synth
+    threads = oracle.cpu_count()
+    shapes = {"qkv": [(4096, 3072), (1024, 3072), (1024, 3072)], "wo": [(3072, 4096)],
+              "w13": [(9216, 3072), (9216, 3072)], "w2": [(3072, 9216)]}
+    packed = []
+    for name in mats:
+        blocks = [oracle.quantize(synth.np_weights(n, k, seed=synth.seed_for(2, 0, i)))[0]
+                  for i, (n, k) in enumerate(shapes[name])]
+        W = np.concatenate(blocks, axis=0)
+        n = W.shape[0]
+        k = shapes[name][0][1]
+        packed.append((W, n, k, synth.np_activations(1, k, seed=synth.activation_seed(2000))))
+    done_bytes, t0, reps = 0, time.perf_counter(), 0
+    while True:
+        for W, n, k, x in packed:
+            oracle.matmul(W, n, k, x, nthreads=threads)
+            done_bytes += W.nbytes
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or reps >= 50:
+            break
+    return {"value": done_bytes / el / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"decoder layer 0 linears ({'+'.join(mats)}), {reps} pass(es), "
+                      f"{done_bytes / 1e9:.2f} GB of Q4 weights in {el:.1f} s, fp64 sums, "
+                      f"{threads} threads"}
+
+
+def run_reference(args):
+    world, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    import numpy as np
+
+    import oracle
+    import synth
+    threads = oracle.cpu_count()
+    blocks = [oracle.quantize(synth.np_weights(n, 3072, seed=synth.seed_for(2, 0, i)))[0]
+              for i, n in enumerate((4096, 1024, 1024))]
+    W = np.concatenate(blocks, axis=0)
+    n, k = W.shape[0], 3072
+    xs = [synth.np_activations(1, k, seed=synth.activation_seed(2000, s))
+          for s in range(min(args.steps + args.warmup, 64))]
+    for s in range(args.warmup):
+        oracle.matmul(W, n, k, xs[s % len(xs)], nthreads=threads)
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        oracle.matmul(W, n, k, xs[s % len(xs)], nthreads=threads)
+    el = time.perf_counter() - t0
+    value = W.nbytes * args.steps / el / 1e9
+    sample = (f"one decoder layer's [wq;wk;wv] product (6144x3072 Q4_0, {W.nbytes} B) per "
+              f"step, fp64 sums, {threads} threads")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "reference_step": sample},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def _time_graph_replays(graphs, stream, torch):
+    """Replay (graph, count) pairs back to back; return device ms."""
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for g, cnt in graphs:
+            for _ in range(cnt):
+                g.replay()
+        e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1)
+
+
+def run_ours(args):
+    import torch
+
+    import synth
+    from bit_weight_quantized_03_b300 import (FLAG_PDL, Workspace, lib, q4_embed_gather,
+                                              q4_gemv, q4_quantize)
+    from bit_weight_quantized_03_b300.stacks import DecoderStack, EncoderStack
+
+    world, rank, local = _dist()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    lib()
+    hbm, bf16_burst, bf16_sust, peak_src = _peaks()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.Stream()
+
+    # ---------------- decoder stack (headline)
+    dec = DecoderStack(device=dev)
+    wbytes = dec.weight_bytes()
+    abytes = dec.activation_bytes()
+    G = 8
+    n_inputs = G
+    inputs = [synth.torch_activations(1, 3072, seed=synth.activation_seed(2000, s), device=dev)
+              for s in range(n_inputs)]
+    g_multi = dec.capture(inputs, stream)
+    g_one = dec.capture(inputs[:1], stream)
+
+    def plan(steps):
+        return [(g_multi, steps // G), (g_one, steps % G)]
+
+    _time_graph_replays(plan(max(args.warmup, 3)), stream, torch)
+    torch.cuda.synchronize()
+    _barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        ms = _time_graph_replays(plan(args.steps), stream, torch)
+    torch.cuda.synchronize()
+    ms = _barrier_max(ms, world, torch)
+    ms_step = ms / args.steps
+    value = world * wbytes * args.steps / (ms * 1e-3) / 1e9
+    achieved = (wbytes + abytes) / (ms_step * 1e-3) / 1e9
+    clocks = clk.summary()
+
+    # ---------------- e2e: host input -> step -> host output, every step
+    x_host = torch.empty((args.steps, 3072), dtype=torch.float32).pin_memory()
+    x_host.copy_(torch.randn((args.steps, 3072), generator=torch.Generator().manual_seed(7)))
+    y_host = torch.empty((args.steps, 3072), dtype=torch.float32).pin_memory()
+    x_dev = torch.empty((1, 3072), dtype=torch.float32, device=dev)
+    g_e2e = dec.capture([x_dev], stream)
+    with torch.cuda.stream(stream):
+        for s in range(3):
+            x_dev.copy_(x_host[s:s + 1], non_blocking=True)
+            g_e2e.replay()
+            y_host[s:s + 1].copy_(dec.x, non_blocking=True)
+    stream.synchronize()
+    _barrier(world)
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for s in range(args.steps):
+            x_dev.copy_(x_host[s:s + 1], non_blocking=True)
+            g_e2e.replay()
+            y_host[s:s + 1].copy_(dec.x, non_blocking=True)
+    stream.synchronize()
+    e2e_s = _barrier_max(time.perf_counter() - t0, world, torch)
+    e2e = {"value": world * wbytes * args.steps / e2e_s / 1e9, "unit": "GB/s",
+           "h2d_bytes_per_step": 3072 * 4, "d2h_bytes_per_step": 3072 * 4,
+           "ms_per_step": e2e_s / args.steps * 1e3}
+    del g_e2e
+
+    # ---------------- output head GEMV and embedding gather (131072 x 3072 table)
+    extra = {}
+    if not args.skip_extra:
+        V, H = synth.VOCAB, 3072
+        table = torch.empty((V, H // 32 * 18), dtype=torch.uint8, device=dev)
+        for r0 in range(0, V, 16384):
+            w = synth.torch_weights(16384, H, seed=synth.seed_for(3, 0, r0 // 16384), device=dev)
+            q4_quantize(w, blocks=table[r0:r0 + 16384])
+            del w
+        xh = synth.torch_activations(1, H, seed=synth.activation_seed(3000), device=dev)
+        logits = torch.empty((1, V), device=dev)
+        ws = Workspace(dev)
+        reps = 20
+        gh = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            q4_gemv(table, V, H, xh, y=logits, workspace=ws, stream=stream)
+            stream.synchronize()
+            with torch.cuda.graph(gh, stream=stream):
+                for _ in range(reps):
+                    q4_gemv(table, V, H, xh, y=logits, workspace=ws, flags=FLAG_PDL,
+                            stream=stream)
+        _time_graph_replays([(gh, 2)], stream, torch)
+        hms = _time_graph_replays([(gh, 3)], stream, torch) / (3 * reps)
+        head_bytes = table.numel()
+        extra["head_gemv"] = {"workload": "output head 3072->131072, batch 1",
+                              "us_per_call": hms * 1e3,
+                              "weight_gbs": head_bytes / (hms * 1e-3) / 1e9,
+                              "frac_of_hbm": head_bytes / (hms * 1e-3) / 1e9 / hbm,
+                              "note": "226 MB table > L2; consecutive calls re-read it"}
+        gather = {}
+        for B in (1, 64, 4096):
+            ids = synth.torch_token_ids(B, V, seed=B, device=dev)
+            out = torch.empty((B, H), device=dev)
+            gg = torch.cuda.CUDAGraph()
+            r = 50 if B < 4096 else 20
+            with torch.cuda.stream(stream):
+                q4_embed_gather(table, V, H, ids, out=out, stream=stream)
+                stream.synchronize()
+                with torch.cuda.graph(gg, stream=stream):
+                    for _ in range(r):
+                        q4_embed_gather(table, V, H, ids, out=out, stream=stream)
+            _time_graph_replays([(gg, 2)], stream, torch)
+            gms = _time_graph_replays([(gg, 3)], stream, torch) / (3 * r)
+            nbytes = B * (H // 32 * 18 + H * 4 + 4)
+            gather[str(B)] = {"us_per_call": gms * 1e3, "gbs": nbytes / (gms * 1e-3) / 1e9}
+        extra["embed_gather"] = gather
+        del table, gh
+
+    # ---------------- prefill / encoder GEMM
+    gemm = None
+    if not args.skip_gemm:
+        M = 3000
+        try:
+            enc = EncoderStack(frames=M, device=dev)
+            x0 = synth.torch_activations(M, 1280, seed=synth.activation_seed(4000), device=dev,
+                                         dtype=torch.bfloat16)
+            ge = enc.capture(x0, stream)
+            _time_graph_replays([(ge, 2)], stream, torch)
+            _barrier(world)
+            gms = _barrier_max(_time_graph_replays([(ge, 5)], stream, torch) / 5, world, torch)
+            tflops = enc.flops_per_pass() / (gms * 1e-3) / 1e12
+            gemm = {"workload": f"encoder linear stack, 32 layers x (qkv 1280->3840, out "
+                                f"1280->1280, up 1280->5120, down 5120->1280), M={M} frames",
+                    "value": world * tflops, "unit": "TFLOP/s", "ms_per_pass": gms,
+                    "roofline": {"bound": "tensor", "achieved": tflops, "peak": bf16_burst,
+                                 "unit": "TFLOP/s", "frac": tflops / bf16_burst,
+                                 "peak_source": f"{peak_src} bf16 burst"},
+                    "frac_of_sustained": tflops / bf16_sust,
+                    "gpu_launches_per_pass": enc.launches_per_pass()}
+            del enc, ge
+        except Exception as e:  # reported, never silently replaced
+            gemm = {"error": f"{type(e).__name__}: {e}"}
+
+    cpu = _oracle_sample(seconds=args.cpu_seconds) if rank == 0 and world == 1 else None
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp32",
+        "data": "synthetic (seeded N(0,0.02^2) weights quantized on device, N(0,1) activations)",
+        "config": {"workload": WORKLOAD, "layers": dec.layers, "hidden": 3072,
+                   "gqa": "32Q/8KV", "ffn": 9216, "batch": 1,
+                   "weight_bytes_per_step": wbytes, "activation_bytes_per_step": abytes,
+                   "l2": "inputs larger than L2: 1.70 GB of weights per step vs 126 MB L2",
+                   "graph": f"CUDA graphs of {G} steps (PDL between the 104 GEMVs of a step)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "traffic": args.traffic,
+                     "kernel": "gemv_stream_kernel<1>",
+                     "peak_source": f"{peak_src} HBM copy bandwidth",
+                     "per_launch": "algorithmic bytes of the 104 launches of a step / step time"},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": dec.launches_per_step() * args.steps,
+        "clocks": clocks,
+        "prefill_gemm": gemm,
+    }
+    line.update(extra)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=256)
+    ap.add_argument("--warmup", type=int, default=16)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--skip-gemm", action="store_true")
+    ap.add_argument("--skip-extra", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="per-launch DRAM bytes of the GEMV kernel from an ncu capture")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,188 @@
+// q4_api.cu -- the extern "C" entry points declared in include/q4.h: argument
+// and alignment checks (nothing is launched when they fail), workspace sizing,
+// the batch-size crossover of q4_linear, and the kernel launches.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "../../include/q4.h"
+#include "q4_internal.h"
+
+namespace q4 {
+
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cached[dev] == 0) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+      v = 148;
+    cached[dev] = v;
+  }
+  return cached[dev];
+}
+
+}  // namespace q4
+
+namespace {
+
+inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+inline q4_status from_cuda(cudaError_t e) { return e == cudaSuccess ? Q4_OK : Q4_ERR_CUDA; }
+
+// Largest product sizes the kernels index with their 64-bit offsets; far above
+// anything that fits in device memory, so these only catch garbage arguments.
+constexpr int64_t kMaxDim = int64_t(1) << 40;
+
+q4_status check_matrix(const void* W, int64_t n, int64_t k) {
+  if (W == nullptr || n <= 0 || k <= 0 || n > kMaxDim || k > kMaxDim) return Q4_ERR_INVALID_ARG;
+  if (k % Q4_BLOCK_ELEMS != 0) return Q4_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(W, 16)) return Q4_ERR_MISALIGNED;
+  return Q4_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* q4_version(void) { return "q4-b300 0.1 (sm_103a)"; }
+
+const char* q4_status_string(q4_status st) {
+  switch (st) {
+    case Q4_OK: return "ok";
+    case Q4_ERR_INVALID_ARG: return "invalid argument";
+    case Q4_ERR_MISALIGNED: return "misaligned pointer or leading dimension";
+    case Q4_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case Q4_ERR_NONFINITE: return "non-finite input or binary16 scale overflow";
+    case Q4_ERR_ID_OUT_OF_RANGE: return "token id out of range";
+    case Q4_ERR_TIMEOUT: return "bounded wait in a kernel ran out";
+    case Q4_ERR_CUDA: return "CUDA error";
+    case Q4_ERR_WORKSPACE: return "workspace missing or too small";
+  }
+  return "unknown status";
+}
+
+q4_status q4_quantize(const float* w, int64_t n, int64_t k, void* blocks, int32_t* status_dev,
+                      q4_stream_t s) {
+  if (w == nullptr || blocks == nullptr || n <= 0 || k <= 0 || n > kMaxDim || k > kMaxDim)
+    return Q4_ERR_INVALID_ARG;
+  if (k % Q4_BLOCK_ELEMS != 0) return Q4_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(w, 16) || !aligned(blocks, 16)) return Q4_ERR_MISALIGNED;
+  return from_cuda(q4::quantize_launch(w, n, k, static_cast<uint8_t*>(blocks), status_dev,
+                                       reinterpret_cast<cudaStream_t>(s)));
+}
+
+q4_status q4_dequant_rows(const void* blocks, int64_t row0, int64_t n_rows, int64_t k, void* out,
+                          q4_dtype out_dtype, q4_stream_t s) {
+  q4_status st = check_matrix(blocks, n_rows, k);
+  if (st != Q4_OK) return st;
+  if (out == nullptr || row0 < 0 || row0 > kMaxDim) return Q4_ERR_INVALID_ARG;
+  if (out_dtype != Q4_F32 && out_dtype != Q4_BF16) return Q4_ERR_INVALID_ARG;
+  if (!aligned(out, 16)) return Q4_ERR_MISALIGNED;
+  return from_cuda(q4::dequant_rows_launch(static_cast<const uint8_t*>(blocks), row0, n_rows, k,
+                                           out, out_dtype == Q4_BF16,
+                                           reinterpret_cast<cudaStream_t>(s)));
+}
+
+size_t q4_gemv_workspace_bytes(int64_t n, int64_t k, int64_t m) {
+  if (n <= 0 || k <= 0 || k % Q4_BLOCK_ELEMS || m <= 0 || m > Q4_GEMV_MAX_M) return 0;
+  return q4::gemv_plan(n, k, m).ws_bytes;
+}
+
+q4_status q4_gemv(const void* W, int64_t n, int64_t k, const float* x, int64_t m, int64_t ldx,
+                  float* y, int64_t ldy, void* workspace, size_t ws_bytes, int32_t* status_dev,
+                  uint32_t flags, q4_stream_t s) {
+  q4_status st = check_matrix(W, n, k);
+  if (st != Q4_OK) return st;
+  if (x == nullptr || y == nullptr || m <= 0 || ldx < k || ldy < n) return Q4_ERR_INVALID_ARG;
+  if (m > Q4_GEMV_MAX_M) return Q4_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(x, 16) || ldx % 4 != 0 || !aligned(y, 4)) return Q4_ERR_MISALIGNED;
+  const q4::GemvPlan plan = q4::gemv_plan(n, k, m);
+  if (plan.ws_bytes > 0 && (workspace == nullptr || ws_bytes < plan.ws_bytes))
+    return Q4_ERR_WORKSPACE;
+  if (plan.ws_bytes > 0 && !aligned(workspace, 16)) return Q4_ERR_MISALIGNED;
+  return from_cuda(q4::gemv_launch(plan, static_cast<const uint8_t*>(W), n, k, x, m, ldx, y, ldy,
+                                   workspace, status_dev, flags, reinterpret_cast<cudaStream_t>(s)));
+}
+
+size_t q4_gemm_workspace_bytes(int64_t n, int64_t k, int64_t m) {
+  if (n <= 0 || k <= 0 || k % 256 || m <= 0) return 0;
+  return q4::gemm_plan(n, k, m).ws_bytes;
+}
+
+q4_status q4_gemm(const void* W, int64_t n, int64_t k, const void* X, int64_t m, int64_t ldx,
+                  void* Y, q4_dtype y_dtype, int64_t ldy, void* workspace, size_t ws_bytes,
+                  int32_t* status_dev, uint32_t flags, q4_stream_t s) {
+  q4_status st = check_matrix(W, n, k);
+  if (st != Q4_OK) return st;
+  if (X == nullptr || Y == nullptr || m <= 0 || m > kMaxDim || ldx < k || ldy < n)
+    return Q4_ERR_INVALID_ARG;
+  if (y_dtype != Q4_F32 && y_dtype != Q4_BF16) return Q4_ERR_INVALID_ARG;
+  if (k % 256 != 0) return Q4_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(X, 16) || ldx % 8 != 0 || !aligned(Y, 16)) return Q4_ERR_MISALIGNED;
+  if (y_dtype == Q4_F32 ? (ldy % 4 != 0) : (ldy % 8 != 0)) return Q4_ERR_MISALIGNED;
+  const q4::GemmPlan plan = q4::gemm_plan(n, k, m);
+  if (plan.ws_bytes > 0 && (workspace == nullptr || ws_bytes < plan.ws_bytes))
+    return Q4_ERR_WORKSPACE;
+  if (plan.ws_bytes > 0 && !aligned(workspace, 16)) return Q4_ERR_MISALIGNED;
+  cudaError_t e = q4::gemm_launch(plan, static_cast<const uint8_t*>(W), n, k, X, m, ldx, Y,
+                                  y_dtype == Q4_BF16, ldy, workspace, status_dev, flags,
+                                  reinterpret_cast<cudaStream_t>(s));
+  if (e == cudaErrorNotSupported) return Q4_ERR_UNSUPPORTED_SHAPE;
+  return from_cuda(e);
+}
+
+q4_status q4_embed_gather(const void* table, int64_t vocab, int64_t k, const int32_t* ids,
+                          int64_t n_ids, float* out, int32_t* status_dev, q4_stream_t s) {
+  q4_status st = check_matrix(table, vocab, k);
+  if (st != Q4_OK) return st;
+  if (ids == nullptr || out == nullptr || n_ids <= 0 || n_ids > kMaxDim) return Q4_ERR_INVALID_ARG;
+  if (!aligned(ids, 4) || !aligned(out, 16)) return Q4_ERR_MISALIGNED;
+  return from_cuda(q4::embed_gather_launch(static_cast<const uint8_t*>(table), vocab, k, ids, n_ids,
+                                           out, status_dev, reinterpret_cast<cudaStream_t>(s)));
+}
+
+int64_t q4_linear_crossover_m(int64_t n, int64_t k) {
+  (void)n;
+  // Largest batch still sent to the fp32 GEMV.  Measured on B300 for the
+  // decoder shapes (see the crossover sweep); the tensor-core path needs
+  // k % 256 == 0.
+  if (k % 256 != 0) return Q4_GEMV_MAX_M;
+  return 4;
+}
+
+size_t q4_linear_workspace_bytes(int64_t n, int64_t k, int64_t m, q4_dtype x_dtype) {
+  if (n <= 0 || k <= 0 || k % Q4_BLOCK_ELEMS || m <= 0) return 0;
+  if (x_dtype == Q4_F32 && m <= q4_linear_crossover_m(n, k)) return q4_gemv_workspace_bytes(n, k, m);
+  size_t bytes = q4_gemm_workspace_bytes(n, k, m);
+  if (x_dtype == Q4_F32) bytes = (bytes + 255) / 256 * 256 + static_cast<size_t>(m) * k * 2;
+  return bytes;
+}
+
+q4_status q4_linear(const void* W, int64_t n, int64_t k, const void* X, q4_dtype x_dtype, int64_t m,
+                    int64_t ldx, float* Y, int64_t ldy, void* workspace, size_t ws_bytes,
+                    int32_t* status_dev, uint32_t flags, q4_stream_t s) {
+  q4_status st = check_matrix(W, n, k);
+  if (st != Q4_OK) return st;
+  if (X == nullptr || Y == nullptr || m <= 0 || ldx < k || ldy < n) return Q4_ERR_INVALID_ARG;
+  if (x_dtype != Q4_F32 && x_dtype != Q4_BF16) return Q4_ERR_INVALID_ARG;
+  if (x_dtype == Q4_F32 && m <= q4_linear_crossover_m(n, k))
+    return q4_gemv(W, n, k, static_cast<const float*>(X), m, ldx, Y, ldy, workspace, ws_bytes,
+                   status_dev, flags, s);
+  if (x_dtype == Q4_BF16)
+    return q4_gemm(W, n, k, X, m, ldx, Y, Q4_F32, ldy, workspace, ws_bytes, status_dev, flags, s);
+  // fp32 activations on the tensor-core path: round them to bf16 first
+  if (!aligned(X, 16) || ldx % 4 != 0) return Q4_ERR_MISALIGNED;
+  const size_t need = q4_linear_workspace_bytes(n, k, m, x_dtype);
+  if (workspace == nullptr || ws_bytes < need) return Q4_ERR_WORKSPACE;
+  const size_t gemm_ws = (q4_gemm_workspace_bytes(n, k, m) + 255) / 256 * 256;
+  void* xb = static_cast<uint8_t*>(workspace) + gemm_ws;
+  cudaError_t e = q4::f32_to_bf16_launch(static_cast<const float*>(X), m, k, ldx, xb, k,
+                                         reinterpret_cast<cudaStream_t>(s));
+  if (e != cudaSuccess) return Q4_ERR_CUDA;
+  return q4_gemm(W, n, k, xb, m, k, Y, Q4_F32, ldy, workspace, gemm_ws, status_dev,
+                 flags & ~Q4_FLAG_PDL, s);
+}
+
+}  // extern "C"

@@ -1,0 +1,55 @@
+// q4_internal.h -- declarations shared between the C-ABI host code (q4_api.cu)
+// and the kernel files.  Not part of the public interface (that is include/q4.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace q4 {
+
+// Wall-clock limit of every bounded wait inside a kernel (nanoseconds).
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s
+
+// Internal flag: tests make one bounded wait run out on purpose (see
+// gemv_launch); never set by the public API.
+constexpr uint32_t kFlagTestStallOneWait = 1u << 30;
+
+// --------------------------------------------------------------- elementwise
+cudaError_t dequant_rows_launch(const uint8_t* blocks, int64_t row0, int64_t n_rows, int64_t k,
+                                void* out, bool out_bf16, cudaStream_t s);
+cudaError_t embed_gather_launch(const uint8_t* table, int64_t vocab, int64_t k, const int32_t* ids,
+                                int64_t n_ids, float* out, int32_t* status, cudaStream_t s);
+cudaError_t quantize_launch(const float* w, int64_t n, int64_t k, uint8_t* blocks,
+                            int32_t* status, cudaStream_t s);
+cudaError_t f32_to_bf16_launch(const float* x, int64_t m, int64_t k, int64_t ldx, void* out,
+                               int64_t ldo, cudaStream_t s);
+
+// --------------------------------------------------------------- GEMV
+struct GemvPlan {
+  bool fast;          // streamed kernel (k % 256 == 0) vs the generic one
+  int64_t units;      // (32-row group, 256-wide k slice) pairs
+  int64_t warps;      // workers the units are split over
+  int64_t groups;     // 32-row groups
+  size_t ws_bytes;    // workspace the plan needs
+};
+GemvPlan gemv_plan(int64_t n, int64_t k, int64_t m);
+cudaError_t gemv_launch(const GemvPlan& plan, const uint8_t* W, int64_t n, int64_t k,
+                        const float* x, int64_t m, int64_t ldx, float* y, int64_t ldy,
+                        void* workspace, int32_t* status, uint32_t flags, cudaStream_t s);
+
+// --------------------------------------------------------------- GEMM (tcgen05)
+struct GemmPlan {
+  int64_t n_tiles, m_tiles, splits;
+  int block_n;        // tokens per tile (MMA N)
+  size_t ws_bytes;
+};
+GemmPlan gemm_plan(int64_t n, int64_t k, int64_t m);
+cudaError_t gemm_launch(const GemmPlan& plan, const uint8_t* W, int64_t n, int64_t k,
+                        const void* X, int64_t m, int64_t ldx, void* Y, bool y_bf16,
+                        int64_t ldy, void* workspace, int32_t* status, uint32_t flags,
+                        cudaStream_t s);
+
+int sm_count();
+
+}  // namespace q4

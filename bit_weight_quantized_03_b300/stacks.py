@@ -1,0 +1,191 @@
+"""The Q4_0 linear stacks of the Voxtral Mini 4B Realtime port, run through the
+library's public calls.
+
+GeekNews (es.news.hada.io/topic?id=26595, "Arquitectura") gives the shapes:
+a 26-layer decoder with hidden size 3072 and GQA 32Q/8KV (q 4096 = 32 x 128,
+k and v 1024 = 8 x 128), and a 32-layer, 1280-wide causal audio encoder; on the
+quantized path every one of these linears is GGUF Q4_0.  FFN widths 9216
+(decoder) and 5120 (encoder) are assumptions that fit the parameter counts on
+the usedby.ai post ("Bajo el capó": 3.4B LM + 0.6B encoder).
+
+Only the linears are here: attention, norms and activations are outside the
+Q4 path.  Where they would sit, the next linear reads the previous linear's
+output directly (the q rows stand in for the attention output feeding wo, the
+w1 rows for the gated FFN activation feeding w2), which keeps the per-layer
+chain of dependent products that a real decode step has.
+
+Layout in HBM: per decoder layer three row-concatenated matrices that share an
+input -- Wqkv = [wq; wk; wv] (6144 x 3072), W13 = [w1; w3] (18432 x 3072) --
+plus wo (3072 x 4096) and w2 (3072 x 9216), each a contiguous run of Q4_0 rows.
+A decode step is 4 dependent GEMV launches per layer (104 per step) with
+programmatic dependent launch between them, captured in a CUDA graph.
+"""
+from __future__ import annotations
+
+import synth
+
+from . import FLAG_PDL, Workspace, q4_gemm, q4_gemv, q4_quantize
+
+
+def _quantize_rows(parts, k, device, torch):
+    """Quantize several [n_i, k] fp32 matrices into one row-concatenated Q4 matrix."""
+    n_total = sum(p[0] for p in parts)
+    blocks = torch.empty((n_total, k // 32 * 18), dtype=torch.uint8, device=device)
+    r0 = 0
+    st = torch.zeros(1, dtype=torch.int32, device=device)
+    for n, seed in parts:
+        w = synth.torch_weights(n, k, seed=seed, device=device)
+        q4_quantize(w, blocks=blocks[r0:r0 + n], status=st)
+        del w
+        r0 += n
+    return blocks, st
+
+
+class DecoderStack:
+    """26 decoder layers of Q4_0 linears at one token per step."""
+
+    HIDDEN, QDIM, KVDIM, FFN = 3072, 4096, 1024, 9216
+
+    def __init__(self, layers: int = synth.DECODER_LAYERS, config_id: int = 2, device="cuda"):
+        import torch
+        self.torch = torch
+        self.device = torch.device(device)
+        self.layers = layers
+        H, Q, KV, F = self.HIDDEN, self.QDIM, self.KVDIM, self.FFN
+        self.shapes = {"qkv": (Q + 2 * KV, H), "wo": (H, Q), "w13": (2 * F, H), "w2": (H, F)}
+        self.W = []
+        status = []
+        for l in range(layers):
+            s = lambda i: synth.seed_for(config_id, l, i)  # noqa: E731  wq..w2 = 0..6
+            qkv, st1 = _quantize_rows([(Q, s(0)), (KV, s(1)), (KV, s(2))], H, self.device, torch)
+            wo, st2 = _quantize_rows([(H, s(3))], Q, self.device, torch)
+            w13, st3 = _quantize_rows([(F, s(4)), (F, s(5))], H, self.device, torch)
+            w2, st4 = _quantize_rows([(H, s(6))], F, self.device, torch)
+            self.W.append({"qkv": qkv, "wo": wo, "w13": w13, "w2": w2})
+            status += [st1, st2, st3, st4]
+        torch.cuda.synchronize()
+        if any(int(st.item()) != 0 for st in status):
+            raise RuntimeError("quantizing the decoder weights reported a device error")
+        self.y_qkv = torch.empty((1, Q + 2 * KV), device=self.device)
+        self.y_o = torch.empty((1, H), device=self.device)
+        self.y_13 = torch.empty((1, 2 * F), device=self.device)
+        self.x = torch.empty((1, H), device=self.device)
+        self.ws = Workspace(self.device)
+        for name, (n, k) in self.shapes.items():  # size the shared workspace once
+            from . import q4_gemv_workspace_bytes
+            self.ws.get(q4_gemv_workspace_bytes(n, k, 1))
+        self.graphs = {}
+
+    # bytes the method must move per decode step (weights once + activations)
+    def weight_bytes(self) -> int:
+        return sum(int(w.numel()) for layer in self.W for w in layer.values())
+
+    def activation_bytes(self) -> int:
+        per_layer = 0
+        for n, k in self.shapes.values():
+            per_layer += 4 * (k + n)
+        return per_layer * self.layers
+
+    def launches_per_step(self) -> int:
+        return 4 * self.layers
+
+    def _layer(self, l, x_in, stream):
+        W, (nq, h), = self.W[l], self.shapes["qkv"]
+        q4_gemv(W["qkv"], nq, h, x_in, y=self.y_qkv, workspace=self.ws, flags=FLAG_PDL,
+                stream=stream)
+        q4_gemv(W["wo"], h, self.QDIM, self.y_qkv[:, :self.QDIM], y=self.y_o, workspace=self.ws,
+                flags=FLAG_PDL, stream=stream)
+        q4_gemv(W["w13"], 2 * self.FFN, h, self.y_o, y=self.y_13, workspace=self.ws,
+                flags=FLAG_PDL, stream=stream)
+        q4_gemv(W["w2"], h, self.FFN, self.y_13[:, :self.FFN], y=self.x, workspace=self.ws,
+                flags=FLAG_PDL, stream=stream)
+
+    def step(self, x_in, stream=None):
+        """One decode step on the device: x_in [1, 3072] fp32 -> self.x [1, 3072]."""
+        self._layer(0, x_in, stream)
+        for l in range(1, self.layers):
+            self._layer(l, self.x, stream)
+        return self.x
+
+    def capture(self, inputs, stream):
+        """CUDA graph of len(inputs) consecutive steps, step i reading inputs[i]."""
+        torch = self.torch
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            self.step(inputs[0], stream)  # warm the path outside capture
+            stream.synchronize()
+            with torch.cuda.graph(g, stream=stream):
+                for x_in in inputs:
+                    self.step(x_in, stream)
+        return g
+
+
+class EncoderStack:
+    """32 encoder layers of Q4_0 linears over M audio frames (bf16 activations)."""
+
+    DIM, FFN = 1280, 5120
+
+    def __init__(self, frames: int, layers: int = synth.ENCODER_LAYERS, config_id: int = 4,
+                 device="cuda"):
+        import torch
+        self.torch = torch
+        self.device = torch.device(device)
+        self.layers, self.m = layers, frames
+        D, F = self.DIM, self.FFN
+        self.shapes = {"qkv": (3 * D, D), "out": (D, D), "up": (F, D), "down": (D, F)}
+        self.W = []
+        status = []
+        for l in range(layers):
+            s = lambda i: synth.seed_for(config_id, l, i)  # noqa: E731  qkv..down = 0..3
+            qkv, a = _quantize_rows([(3 * D, s(0))], D, self.device, torch)
+            out, b = _quantize_rows([(D, s(1))], D, self.device, torch)
+            up, c = _quantize_rows([(F, s(2))], D, self.device, torch)
+            down, d = _quantize_rows([(D, s(3))], F, self.device, torch)
+            self.W.append({"qkv": qkv, "out": out, "up": up, "down": down})
+            status += [a, b, c, d]
+        torch.cuda.synchronize()
+        if any(int(st.item()) != 0 for st in status):
+            raise RuntimeError("quantizing the encoder weights reported a device error")
+        bf = torch.bfloat16
+        self.y_qkv = torch.empty((frames, 3 * D), dtype=bf, device=self.device)
+        self.y_out = torch.empty((frames, D), dtype=bf, device=self.device)
+        self.y_up = torch.empty((frames, F), dtype=bf, device=self.device)
+        self.x = torch.empty((frames, D), dtype=bf, device=self.device)
+        self.ws = Workspace(self.device)
+
+    def flops_per_pass(self) -> int:
+        return 2 * self.m * self.layers * sum(n * k for n, k in self.shapes.values())
+
+    def weight_bytes(self) -> int:
+        return sum(int(w.numel()) for layer in self.W for w in layer.values())
+
+    def launches_per_pass(self) -> int:
+        return 4 * self.layers
+
+    def _layer(self, l, x_in, stream):
+        W, D, F = self.W[l], self.DIM, self.FFN
+        q4_gemm(W["qkv"], 3 * D, D, x_in, Y=self.y_qkv, workspace=self.ws, flags=FLAG_PDL,
+                stream=stream)
+        q4_gemm(W["out"], D, D, self.y_qkv[:, :D], Y=self.y_out, workspace=self.ws,
+                flags=FLAG_PDL, stream=stream)
+        q4_gemm(W["up"], F, D, self.y_out, Y=self.y_up, workspace=self.ws, flags=FLAG_PDL,
+                stream=stream)
+        q4_gemm(W["down"], D, F, self.y_up, Y=self.x, workspace=self.ws, flags=FLAG_PDL,
+                stream=stream)
+
+    def forward(self, x_in, stream=None):
+        self._layer(0, x_in, stream)
+        for l in range(1, self.layers):
+            self._layer(l, self.x, stream)
+        return self.x
+
+    def capture(self, x_in, stream, passes: int = 1):
+        torch = self.torch
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            self.forward(x_in, stream)
+            stream.synchronize()
+            with torch.cuda.graph(g, stream=stream):
+                for _ in range(passes):
+                    self.forward(x_in, stream)
+        return g

@@ -1,0 +1,162 @@
+/*
+ * q4.h -- C ABI of the GGUF Q4_0 weight-only-quantized linear layer on NVIDIA
+ * B300 (sm_103a).  Library: bit_weight_quantized_03_b300/libq4.so.
+ *
+ * What it computes.  The GeekNews write-up of the Rust/Burn port of Voxtral
+ * Mini 4B Realtime (es.news.hada.io/topic?id=26595) describes a quantized
+ * inference path whose weights are GGUF Q4_0, multiplied by custom GPU shaders
+ * (section "Arquitectura"), and an embedding table kept as Q4 rows that are
+ * looked up per token (section "Soluciones técnicas").  The model shapes come
+ * from the same section: a 26-layer decoder with hidden size 3072 and GQA
+ * 32Q/8KV, and a 32-layer, 1280-wide causal audio encoder.  The calls below are
+ * that layer's operations: quantize, decode, the batch-1 decode product, the
+ * prefill/encoder product and the embedding-row gather.
+ *
+ * Block format (GGUF Q4_0; the pages name it but do not print it):
+ *   32 weights in 18 bytes.  Bytes [0,2): scale d, IEEE binary16, little-endian.
+ *   Bytes [2,18): qs[16]; weight j (0..15) is the low nibble of qs[j], weight
+ *   j+16 the high nibble.  Decoded weight: w = (q - 8) * d, one exact fp32
+ *   multiply (so code 8 with a negative d decodes to -0.0).
+ *   A matrix W with n outputs and reduction length k (k % 32 == 0) is n rows of
+ *   k/32 blocks, rows contiguous: row stride 18*k/32 bytes, "row-major blocks".
+ *
+ * Conventions shared by every call.
+ *   - Pointers are DEVICE pointers owned by the caller, unless a call says
+ *     otherwise.  The library keeps no allocation of its own; scratch space is
+ *     passed in as `workspace`.
+ *   - Every call is asynchronous on stream `s` (NULL = the legacy default
+ *     stream) and never synchronizes the host.
+ *   - Errors the host can see (null pointer, bad size, k % 32 != 0, broken
+ *     alignment, too little workspace) return at once and launch nothing.
+ *   - Errors found on the device are written to the caller's int32 status word
+ *     `status_dev` (device memory, may be NULL): the first error wins (an
+ *     atomic compare-and-swap from Q4_OK), so the caller clears it to 0 before
+ *     the call and reads it after synchronizing.
+ *   - Launch or runtime failures return Q4_ERR_CUDA.
+ *   - Leading dimensions are in elements.
+ *   - Flag Q4_FLAG_PDL lets the kernel be launched as a programmatic dependent
+ *     launch: it may start while the previous kernel on the stream is still
+ *     running and read W early; everything else it reads or writes waits for
+ *     that kernel.  Only set it when the previous kernel does not write W.
+ *   - Workspaces (q4_gemv, q4_gemm, q4_linear) hold split-K partial sums and
+ *     arrival counters.  Zero-fill a workspace once before its first use; every
+ *     call that ends without a device error leaves it zero-filled again.  Calls
+ *     that may run concurrently need separate workspaces.
+ *   - Flag Q4_FLAG_TEST_STALL is for tests only: one bounded wait inside the
+ *     kernel is made to run out, so the call reports Q4_ERR_TIMEOUT in
+ *     status_dev after about a second, part of y is left unwritten, and the
+ *     workspace must be zero-filled again.
+ */
+#ifndef Q4_H
+#define Q4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st* q4_stream_t; /* the same type as cudaStream_t */
+
+typedef enum q4_status {
+  Q4_OK = 0,
+  Q4_ERR_INVALID_ARG = 1,       /* null pointer, size <= 0, bad leading dimension or dtype */
+  Q4_ERR_MISALIGNED = 2,        /* a pointer or leading dimension breaks the call's alignment rule */
+  Q4_ERR_UNSUPPORTED_SHAPE = 3, /* k % 32 != 0, or a size beyond the call's stated limit */
+  Q4_ERR_NONFINITE = 4,         /* device: NaN/Inf input or a binary16 scale overflow in quantize */
+  Q4_ERR_ID_OUT_OF_RANGE = 5,   /* device: a gather id outside [0, vocab) */
+  Q4_ERR_TIMEOUT = 6,           /* device: a bounded wait inside a kernel ran out */
+  Q4_ERR_CUDA = 7,              /* a CUDA runtime call or kernel launch failed */
+  Q4_ERR_WORKSPACE = 8          /* workspace missing or smaller than the *_workspace_bytes() figure */
+} q4_status;
+
+typedef enum q4_dtype { Q4_F32 = 0, Q4_BF16 = 1 } q4_dtype;
+
+#define Q4_BLOCK_ELEMS 32
+#define Q4_BLOCK_BYTES 18
+#define Q4_FLAG_PDL 1u
+#define Q4_FLAG_TEST_STALL (1u << 30)
+#define Q4_GEMV_MAX_M 16 /* largest batch the fp32 GEMV takes */
+
+/* Quantize fp32 weights to Q4_0 blocks.
+ * The pages give no quantizer ("Arquitectura" names only the GGUF Q4_0
+ * format); the rule implemented is: m = first element of largest |x| in the
+ * block; d = binary16(m / -8), round to nearest even (+0 when m = +-0);
+ * dd = float(d); code q = clamp(floor(x/dd + 8.5), 0, 15), every code 8 when
+ * dd == 0; byte j = q[j] | q[j+16] << 4.  Division and add are IEEE fp32.
+ *   w          [n][k] fp32, row-major contiguous, 16-byte aligned.
+ *   blocks     output, n*k/32*18 bytes, 16-byte aligned.
+ *   status_dev a block holding NaN/Inf, or whose d rounds to Inf, is written as
+ *              d = +0 with all codes 8 and sets Q4_ERR_NONFINITE.
+ * n >= 1, k >= 32, k % 32 == 0. */
+q4_status q4_quantize(const float* w, int64_t n, int64_t k, void* blocks,
+                      int32_t* status_dev, q4_stream_t s);
+
+/* Decode rows [row0, row0 + n_rows) of a Q4_0 matrix to fp32 (bit-exact
+ * (q - 8) * d) or bf16 (that fp32 value rounded to nearest even).
+ *   blocks  the matrix base (row 0), 16-byte aligned.
+ *   out     [n_rows][k] contiguous, 16-byte aligned. */
+q4_status q4_dequant_rows(const void* blocks, int64_t row0, int64_t n_rows, int64_t k, void* out,
+                          q4_dtype out_dtype, q4_stream_t s);
+
+/* Batch-1 (and small-batch) decode product, fp32 in and out:
+ *   y[i][r] = sum_j w^[r][j] * x[i][j]   for r < n, i < m
+ * with w^ the decoded weights, accumulated in fp32 (per-element error within
+ * 1e-4 * sum_j |w^[r][j] x[i][j]|).  The decoder's linears (hidden 3072, GQA
+ * 32Q/8KV, "Arquitectura") run through this at one token per step.
+ *   W   [n rows of k/32 blocks], 16-byte aligned.
+ *   x   [m][ldx] fp32, 16-byte aligned, ldx >= k, ldx % 4 == 0.
+ *   y   [m][ldy] fp32, 4-byte aligned, ldy >= n; must not overlap x or W.
+ *   1 <= m <= Q4_GEMV_MAX_M.  The workspace holds split-K partial sums:
+ *   pass at least q4_gemv_workspace_bytes(n, k, m) bytes, 16-byte aligned
+ *   (NULL is fine when that figure is 0).  Results do not depend on timing:
+ *   the partial sums are added in a fixed order.
+ *   status_dev (may be NULL) receives Q4_ERR_TIMEOUT if a bounded wait ran out. */
+q4_status q4_gemv(const void* W, int64_t n, int64_t k, const float* x, int64_t m, int64_t ldx,
+                  float* y, int64_t ldy, void* workspace, size_t ws_bytes, int32_t* status_dev,
+                  uint32_t flags, q4_stream_t s);
+size_t q4_gemv_workspace_bytes(int64_t n, int64_t k, int64_t m);
+
+/* Prefill / audio-encoder product on the tensor cores:
+ *   Y[i][r] = sum_j bf16(w^[r][j]) * X[i][j]   (fp32 accumulation)
+ * for the 32-layer, 1280-wide encoder and prefill ("Arquitectura"); error within
+ * 8e-3 * sum_j |w^[r][j] X[i][j]|.
+ *   W  as for q4_gemv; k % 256 == 0.
+ *   X  [m][ldx] bf16, 16-byte aligned, ldx % 8 == 0, ldx >= k.
+ *   Y  [m][ldy], fp32 (ldy % 4 == 0) or bf16 (ldy % 8 == 0), 16-byte aligned.
+ *   m >= 1.  workspace as for q4_gemv with q4_gemm_workspace_bytes(). */
+q4_status q4_gemm(const void* W, int64_t n, int64_t k, const void* X, int64_t m, int64_t ldx,
+                  void* Y, q4_dtype y_dtype, int64_t ldy, void* workspace, size_t ws_bytes,
+                  int32_t* status_dev, uint32_t flags, q4_stream_t s);
+size_t q4_gemm_workspace_bytes(int64_t n, int64_t k, int64_t m);
+
+/* Q4 embedding-row gather ("Soluciones técnicas": the 1.5 GiB table is kept as
+ * Q4 rows and rows are looked up per token; here the lookup runs on the GPU):
+ *   out[b][:] = decode(table row ids[b])  (fp32, bit-exact)
+ *   table  [vocab rows of k/32 blocks], 16-byte aligned.
+ *   ids    [n_ids] int32 (device).  An id outside [0, vocab) gives a row of
+ *          +0.0 and sets Q4_ERR_ID_OUT_OF_RANGE in status_dev.
+ *   out    [n_ids][k] fp32, 16-byte aligned. */
+q4_status q4_embed_gather(const void* table, int64_t vocab, int64_t k, const int32_t* ids,
+                          int64_t n_ids, float* out, int32_t* status_dev, q4_stream_t s);
+
+/* Linear layer with the batch-size crossover: m <= q4_linear_crossover_m(n, k)
+ * and fp32 X run q4_gemv; otherwise q4_gemm (fp32 X is first rounded to bf16
+ * into the workspace).  Y is fp32 [m][ldy].  X dtype Q4_F32 needs ldx % 4 == 0,
+ * Q4_BF16 needs ldx % 8 == 0.  workspace >= q4_linear_workspace_bytes(). */
+q4_status q4_linear(const void* W, int64_t n, int64_t k, const void* X, q4_dtype x_dtype, int64_t m,
+                    int64_t ldx, float* Y, int64_t ldy, void* workspace, size_t ws_bytes,
+                    int32_t* status_dev, uint32_t flags, q4_stream_t s);
+size_t q4_linear_workspace_bytes(int64_t n, int64_t k, int64_t m, q4_dtype x_dtype);
+int64_t q4_linear_crossover_m(int64_t n, int64_t k);
+
+/* Static strings; never NULL. */
+const char* q4_status_string(q4_status st);
+const char* q4_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* Q4_H */

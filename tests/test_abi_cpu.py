@@ -1,0 +1,133 @@
+"""CPU-only checks of the C ABI: libq4.so loads, exports every entry point that
+include/q4.h declares, and rejects bad arguments on the host (nothing here
+launches a kernel or needs a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "q4.h")
+
+
+@pytest.fixture(scope="module")
+def q4():
+    from bit_weight_quantized_03_b300 import build
+    build.build()
+    import bit_weight_quantized_03_b300 as q4mod
+    return q4mod
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(q4_[a-z0-9_]+)\s*\(", text)))
+
+
+def header_constants():
+    text = open(HEADER).read()
+    consts = {m.group(1): int(m.group(2), 0) for m in
+              re.finditer(r"#define\s+(Q4_\w+)\s+\(?([0-9xu]+?)u?\b", text)}
+    enums = {m.group(1): int(m.group(2)) for m in re.finditer(r"\b(Q4_\w+)\s*=\s*(\d+)", text)}
+    return consts, enums
+
+
+def test_every_declared_symbol_is_exported(q4):
+    names = declared_functions()
+    assert len(names) >= 12, names
+    L = q4.lib()
+    missing = [n for n in names if not hasattr(L, n)]
+    assert not missing, missing
+    from bit_weight_quantized_03_b300._lib import SIGNATURES
+    assert sorted(SIGNATURES) == names
+
+
+def test_constants_match_header(q4):
+    consts, enums = header_constants()
+    assert enums["Q4_OK"] == q4.OK == 0
+    assert enums["Q4_ERR_INVALID_ARG"] == q4.ERR_INVALID_ARG
+    assert enums["Q4_ERR_MISALIGNED"] == q4.ERR_MISALIGNED
+    assert enums["Q4_ERR_UNSUPPORTED_SHAPE"] == q4.ERR_UNSUPPORTED_SHAPE
+    assert enums["Q4_ERR_NONFINITE"] == q4.ERR_NONFINITE
+    assert enums["Q4_ERR_ID_OUT_OF_RANGE"] == q4.ERR_ID_OUT_OF_RANGE
+    assert enums["Q4_ERR_TIMEOUT"] == q4.ERR_TIMEOUT
+    assert enums["Q4_ERR_CUDA"] == q4.ERR_CUDA
+    assert enums["Q4_ERR_WORKSPACE"] == q4.ERR_WORKSPACE
+    assert enums["Q4_F32"] == q4.F32 and enums["Q4_BF16"] == q4.BF16
+    assert consts["Q4_BLOCK_ELEMS"] == 32 and consts["Q4_BLOCK_BYTES"] == 18
+    assert consts["Q4_GEMV_MAX_M"] == q4.GEMV_MAX_M
+    assert consts["Q4_FLAG_PDL"] == q4.FLAG_PDL
+
+
+def test_status_strings(q4):
+    L = q4.lib()
+    for code in range(9):
+        s = L.q4_status_string(code).decode()
+        assert s and s != "unknown status"
+    assert L.q4_status_string(99).decode() == "unknown status"
+    assert b"sm_103a" in L.q4_version()
+
+
+# Fake, never-dereferenced device addresses: validation must reject the call
+# before anything touches them.
+A16 = 0x7F0000000000
+A2 = A16 + 2
+
+
+def test_host_validation_rejects_bad_arguments(q4):
+    L = q4.lib()
+    # null pointers / sizes
+    assert L.q4_gemv(None, 8, 64, A16, 1, 64, A16, 8, None, 0, None, 0, None) == q4.ERR_INVALID_ARG
+    assert L.q4_gemv(A16, 0, 64, A16, 1, 64, A16, 8, None, 0, None, 0, None) == q4.ERR_INVALID_ARG
+    assert L.q4_gemv(A16, 8, 64, A16, 0, 64, A16, 8, None, 0, None, 0, None) == q4.ERR_INVALID_ARG
+    # k not a multiple of 32
+    assert L.q4_gemv(A16, 8, 48, A16, 1, 48, A16, 8, None, 0, None, 0, None) == q4.ERR_UNSUPPORTED_SHAPE
+    # batch above the GEMV limit
+    assert L.q4_gemv(A16, 8, 64, A16, 17, 64, A16, 8, None, 0, None, 0, None) == q4.ERR_UNSUPPORTED_SHAPE
+    # leading dimensions
+    assert L.q4_gemv(A16, 8, 64, A16, 1, 32, A16, 8, None, 0, None, 0, None) == q4.ERR_INVALID_ARG
+    assert L.q4_gemv(A16, 8, 64, A16, 1, 64, A16, 7, None, 0, None, 0, None) == q4.ERR_INVALID_ARG
+    # misalignment
+    assert L.q4_gemv(A2, 8, 64, A16, 1, 64, A16, 8, None, 0, None, 0, None) == q4.ERR_MISALIGNED
+    assert L.q4_gemv(A16, 8, 64, A2, 1, 64, A16, 8, None, 0, None, 0, None) == q4.ERR_MISALIGNED
+    assert L.q4_gemv(A16, 8, 64, A16, 2, 66, A16, 8, None, 0, None, 0, None) == q4.ERR_MISALIGNED
+    # quantize
+    assert L.q4_quantize(None, 2, 64, A16, None, None) == q4.ERR_INVALID_ARG
+    assert L.q4_quantize(A16, 2, 40, A16, None, None) == q4.ERR_UNSUPPORTED_SHAPE
+    assert L.q4_quantize(A2, 2, 64, A16, None, None) == q4.ERR_MISALIGNED
+    # dequant
+    assert L.q4_dequant_rows(A16, 0, 4, 64, None, 0, None) == q4.ERR_INVALID_ARG
+    assert L.q4_dequant_rows(A16, 0, 4, 64, A16, 7, None) == q4.ERR_INVALID_ARG
+    assert L.q4_dequant_rows(A16, -1, 4, 64, A16, 0, None) == q4.ERR_INVALID_ARG
+    assert L.q4_dequant_rows(A16, 0, 4, 64, A2, 0, None) == q4.ERR_MISALIGNED
+    # gather
+    assert L.q4_embed_gather(A16, 10, 64, None, 3, A16, None, None) == q4.ERR_INVALID_ARG
+    assert L.q4_embed_gather(A16, 10, 64, A16, 0, A16, None, None) == q4.ERR_INVALID_ARG
+    assert L.q4_embed_gather(A16, 10, 64, A16 + 1, 3, A16, None, None) == q4.ERR_MISALIGNED
+    # gemm: k must be a multiple of 256, X rows 16-byte aligned
+    assert L.q4_gemm(A16, 8, 288, A16, 4, 288, A16, 0, 8, None, 0, None, 0, None) == q4.ERR_UNSUPPORTED_SHAPE
+    assert L.q4_gemm(A16, 8, 256, A16, 4, 260, A16, 0, 8, None, 0, None, 0, None) == q4.ERR_MISALIGNED
+    assert L.q4_gemm(A16, 8, 256, A16, 4, 256, A16, 5, 8, None, 0, None, 0, None) == q4.ERR_INVALID_ARG
+    # linear: bad dtype
+    assert L.q4_linear(A16, 8, 256, A16, 3, 4, 256, A16, 8, None, 0, None, 0, None) == q4.ERR_INVALID_ARG
+
+
+def test_workspace_sizes_are_consistent(q4):
+    L = q4.lib()
+    assert L.q4_gemv_workspace_bytes(8, 48, 1) == 0          # invalid k
+    assert L.q4_gemv_workspace_bytes(8, 64, 17) == 0         # m above the limit
+    assert L.q4_gemv_workspace_bytes(4096, 288, 1) == 0      # generic kernel: no split-K
+    w1 = L.q4_gemv_workspace_bytes(4096, 3072, 1)
+    w8 = L.q4_gemv_workspace_bytes(4096, 3072, 8)
+    assert 0 < w1 < w8
+    assert L.q4_linear_crossover_m(4096, 3072) >= 1
+    assert L.q4_linear_crossover_m(4096, 288) == q4.GEMV_MAX_M
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    import bit_weight_quantized_03_b300._lib as L
+    monkeypatch.setattr(L, "_lib", None)
+    monkeypatch.setattr(L, "LIB_PATH", str(tmp_path / "absent.so"))
+    with pytest.raises(ImportError):
+        L.lib()
