@@ -122,10 +122,12 @@ def _dist():
 
 
 def _barrier_max(value: float, world: int, torch):
+    """Max of `value` over all ranks (the slowest rank sets the job's time)."""
     if world == 1:
         return value
     import torch.distributed as dist
-    t = torch.tensor([value], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 

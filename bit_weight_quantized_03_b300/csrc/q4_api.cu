@@ -120,8 +120,8 @@ q4_status q4_gemm(const void* W, int64_t n, int64_t k, const void* X, int64_t m,
     return Q4_ERR_INVALID_ARG;
   if (y_dtype != Q4_F32 && y_dtype != Q4_BF16) return Q4_ERR_INVALID_ARG;
   if (k % 256 != 0) return Q4_ERR_UNSUPPORTED_SHAPE;
-  if (!aligned(X, 16) || ldx % 8 != 0 || !aligned(Y, 16)) return Q4_ERR_MISALIGNED;
-  if (y_dtype == Q4_F32 ? (ldy % 4 != 0) : (ldy % 8 != 0)) return Q4_ERR_MISALIGNED;
+  if (!aligned(X, 16) || ldx % 8 != 0) return Q4_ERR_MISALIGNED;
+  if (!aligned(Y, y_dtype == Q4_F32 ? 4 : 2)) return Q4_ERR_MISALIGNED;
   const q4::GemmPlan plan = q4::gemm_plan(n, k, m);
   if (plan.ws_bytes > 0 && (workspace == nullptr || ws_bytes < plan.ws_bytes))
     return Q4_ERR_WORKSPACE;
@@ -181,8 +181,12 @@ q4_status q4_linear(const void* W, int64_t n, int64_t k, const void* X, q4_dtype
   cudaError_t e = q4::f32_to_bf16_launch(static_cast<const float*>(X), m, k, ldx, xb, k,
                                          reinterpret_cast<cudaStream_t>(s));
   if (e != cudaSuccess) return Q4_ERR_CUDA;
-  return q4_gemm(W, n, k, xb, m, k, Y, Q4_F32, ldy, workspace, gemm_ws, status_dev,
-                 flags & ~Q4_FLAG_PDL, s);
+  q4_status st2 = q4_gemm(W, n, k, xb, m, k, Y, Q4_F32, ldy, workspace, gemm_ws, status_dev,
+                          flags & ~Q4_FLAG_PDL, s);
+  if (st2 != Q4_OK) return st2;
+  // hand the workspace back all-zero, as every call promises
+  return from_cuda(cudaMemsetAsync(xb, 0, static_cast<size_t>(m) * k * 2,
+                                   reinterpret_cast<cudaStream_t>(s)));
 }
 
 }  // extern "C"

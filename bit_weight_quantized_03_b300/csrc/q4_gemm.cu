@@ -20,10 +20,6 @@
 // The weight tile is the MMA's M side (128 rows) and the tokens its N side, so
 // one dequantization serves BN tokens.  Every wait is bounded; on expiry the
 // CTA reports Q4_ERR_TIMEOUT, drains its copies and MMAs, frees TMEM and exits.
-#include <cuda.h>
-
-#include <mutex>
-
 #include "q4_device.cuh"
 
 namespace q4 {
@@ -425,25 +421,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------ host side
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, []() {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  });
-  return fn;
-}
-
 int pick_bn(int64_t m) {
   if (m <= 16) return 16;
   if (m <= 32) return 32;
@@ -459,30 +436,16 @@ template <int BN>
 cudaError_t launch_bn(const uint8_t* W, int64_t n, int64_t k, const void* X, int64_t m,
                       int64_t ldx, void* Y, bool y_bf16, int64_t ldy, int32_t* status,
                       bool pdl, cudaStream_t s) {
-  EncodeTiledFn enc = encode_fn();
-  if (enc == nullptr) return cudaErrorNotSupported;
   CUtensorMap tw, tx;
-  {
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(k / 32 * kBlockBytes),
-                                static_cast<cuuint64_t>(n)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(k / 32 * kBlockBytes)};
-    const cuuint32_t box[2] = {kSuperBytes, kTileRows};
-    const cuuint32_t estr[2] = {1, 1};
-    if (enc(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(W), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
-  {
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(m)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldx * 2)};
-    const cuuint32_t box[2] = {kKStep, static_cast<cuuint32_t>(BN)};
-    const cuuint32_t estr[2] = {1, 1};
-    if (enc(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(X), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
+  if (!encode_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, W,
+                      static_cast<uint64_t>(k / 32 * kBlockBytes), static_cast<uint64_t>(n),
+                      static_cast<uint64_t>(k / 32 * kBlockBytes), kSuperBytes, kTileRows,
+                      CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
+  if (!encode_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, static_cast<uint64_t>(k),
+                      static_cast<uint64_t>(m), static_cast<uint64_t>(ldx * 2), kKStep,
+                      static_cast<uint32_t>(BN), CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
   static bool configured[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);

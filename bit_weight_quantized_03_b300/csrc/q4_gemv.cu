@@ -14,10 +14,11 @@
 //     takes one contiguous range of them ("stream-K"), so every warp gets the
 //     same number of units +-1 whatever the shape.
 //   * Each warp streams its units through its own ring of shared-memory slots:
-//     every lane issues one 144-byte cp.async.bulk for its row (evict-first L2
-//     hint), completion counted on the slot's mbarrier.  Slot rows are 144 B
-//     apart (9 x 16 B, odd), so each lane's 16-byte shared loads of its row are
-//     bank-conflict free.  The ring is filled before waiting on the previous
+//     one 2-D TMA tile load per unit (box 144 B x 32 rows over the packed
+//     matrix, evict-first L2 hint), completion counted on the slot's mbarrier.
+//     (Thirty-two 144-byte bulk copies per unit instead were bound by the copy
+//     engine's per-request cost.)  Slot rows are 144 B apart (9 x 16 B, odd), so
+//     each lane's 16-byte shared loads of its row are bank-conflict free.  The ring is filled before waiting on the previous
 //     kernel (programmatic dependent launch), so weight reads overlap the
 //     previous layer's tail.
 //   * Decode: a nibble sitting at bit p <= 16 of a 32-bit word becomes the float
@@ -194,7 +195,8 @@ __device__ __forceinline__ void block_fma(const uint32_t (&r)[36], const float* 
 }
 
 template <int M>
-__global__ void __launch_bounds__(kWarps * 32) gemv_stream_kernel(const StreamParams p) {
+__global__ void __launch_bounds__(kWarps * 32)
+    gemv_stream_kernel(const __grid_constant__ CUtensorMap tmap, const StreamParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t bars[kWarps][kStages];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -216,22 +218,19 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_stream_kernel(const StreamPa
   const uint64_t pol = l2_evict_first_policy();
   const bool stall_test = (p.flags & kFlagTestStallOneWait) != 0 && wid == 0;
 
-  // Issue the copies of unit u into its ring slot (all lanes; one row each).
+  // Issue the TMA load of unit u into its ring slot (lane 0).  Rows past n
+  // arrive zero-filled; the full box is always counted.
   auto issue = [&](int64_t u) {
-    const int64_t g = u / p.nsb, sb = u - g * p.nsb;
-    const int slot = static_cast<int>((u - u0) % kStages);
-    const int64_t row = g * 32 + lane;
-    const int64_t rows = p.n - g * 32 < 32 ? p.n - g * 32 : 32;
-    const uint32_t bar = bar0 + 8 * slot;
     if (lane == 0) {
-      uint32_t bytes = static_cast<uint32_t>(rows) * kSuperBytes;
+      const int64_t g = u / p.nsb, sb = u - g * p.nsb;
+      const int slot = static_cast<int>((u - u0) % kStages);
+      const uint32_t bar = bar0 + 8 * slot;
+      uint32_t bytes = kSlotBytes;
       if (stall_test && u == u0) bytes += 16;  // test hook: this phase never completes
       mbar_arrive_expect_tx(bar, bytes);
+      tma_load_2d_hint(slots + slot * kSlotBytes, &tmap, static_cast<int32_t>(sb * kSuperBytes),
+                       static_cast<int32_t>(g * 32), bar, pol);
     }
-    __syncwarp();
-    if (row < p.n)
-      bulk_g2s(slots + slot * kSlotBytes + lane * kSuperBytes,
-               p.W + row * p.rowbytes + sb * kSuperBytes, kSuperBytes, bar, pol);
   };
 
   int64_t issued = u0;
@@ -349,6 +348,12 @@ constexpr int kCtasPerSm = 2;
 
 template <int M>
 cudaError_t launch_stream(const StreamParams& sp, int64_t grid, bool pdl, cudaStream_t s) {
+  CUtensorMap tmap;
+  if (!encode_tmap_2d(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, sp.W,
+                      static_cast<uint64_t>(sp.rowbytes), static_cast<uint64_t>(sp.n),
+                      static_cast<uint64_t>(sp.rowbytes), kSuperBytes, 32,
+                      CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(gemv_stream_kernel<M>,
@@ -366,7 +371,7 @@ cudaError_t launch_stream(const StreamParams& sp, int64_t grid, bool pdl, cudaSt
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, gemv_stream_kernel<M>, sp);
+  return cudaLaunchKernelEx(&cfg, gemv_stream_kernel<M>, tmap, sp);
 }
 
 template <int M>

@@ -2,6 +2,7 @@
 // and the kernel files.  Not part of the public interface (that is include/q4.h).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -51,5 +52,10 @@ cudaError_t gemm_launch(const GemmPlan& plan, const uint8_t* W, int64_t n, int64
                         cudaStream_t s);
 
 int sm_count();
+
+// 2-D TMA tensor map (cached by address/sizes/strides/box).  false on failure.
+bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t dim0,
+                    uint64_t dim1, uint64_t row_stride_bytes, uint32_t box0, uint32_t box1,
+                    CUtensorMapSwizzle swizzle);
 
 }  // namespace q4

@@ -125,7 +125,7 @@ size_t q4_gemv_workspace_bytes(int64_t n, int64_t k, int64_t m);
  * 8e-3 * sum_j |w^[r][j] X[i][j]|.
  *   W  as for q4_gemv; k % 256 == 0.
  *   X  [m][ldx] bf16, 16-byte aligned, ldx % 8 == 0, ldx >= k.
- *   Y  [m][ldy], fp32 (ldy % 4 == 0) or bf16 (ldy % 8 == 0), 16-byte aligned.
+ *   Y  [m][ldy] fp32 or bf16, aligned to its element size.
  *   m >= 1.  workspace as for q4_gemv with q4_gemm_workspace_bytes(). */
 q4_status q4_gemm(const void* W, int64_t n, int64_t k, const void* X, int64_t m, int64_t ldx,
                   void* Y, q4_dtype y_dtype, int64_t ldy, void* workspace, size_t ws_bytes,

@@ -1,0 +1,305 @@
+"""Parity at the benchmark's full sizes, in the launch configuration the benchmark
+times (CUDA graphs, programmatic dependent launch, shared workspace).
+
+Inputs come from the seeded generators in synth/ (device draws for the large
+cases); expected values come only from the CPU oracle, computed from the same
+generator output (regenerated fp32 weights copied to the host and quantized by
+the oracle).  Where the oracle would take too long on the whole output, rows
+are sampled; properties that hold at any size (exact power-of-two scaling,
+run-to-run determinism, gather = decode of the same rows) cover the rest.
+"""
+import numpy as np
+import pytest
+
+import synth
+from gpu_helpers import bf16_round, same_float, within_tol
+
+pytestmark = pytest.mark.gpu
+GEMV_TOL, GEMM_TOL = 1e-4, 8e-3
+
+
+@pytest.fixture(scope="module")
+def torch():
+    import torch as t
+    assert t.cuda.is_available()
+    return t
+
+
+@pytest.fixture(scope="module")
+def q4():
+    import bit_weight_quantized_03_b300 as m
+    m.lib()
+    return m
+
+
+def _graph_calls(torch, calls):
+    """Run `calls` (callables taking a stream) once inside a captured CUDA graph."""
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        for c in calls:
+            c(s)
+        s.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            for c in calls:
+                c(s)
+    g.replay()
+    torch.cuda.synchronize()
+
+
+def _oracle_rows(oracle_mod, torch, n, k, seed, rows):
+    """Oracle-quantized blocks for `rows` of the seeded [n, k] weight matrix."""
+    w = synth.torch_weights(n, k, seed=seed)[torch.as_tensor(rows, device="cuda")]
+    blocks, rc, _ = oracle_mod.quantize(w.cpu().numpy())
+    assert rc == 0
+    return blocks
+
+
+def _sample_rows(n, count, seed):
+    rng = np.random.default_rng(seed)
+    r = np.unique(np.concatenate([[0, n - 1], rng.integers(0, n, count)]))
+    return r
+
+
+# --------------------------------------------------------------------- config 1
+
+def test_config1_gemv_4096x3072_full(torch, q4, oracle_mod):
+    n, k = 4096, 3072
+    w = synth.np_weights(n, k, seed=synth.seed_for(1))
+    W_ref, rc, _ = oracle_mod.quantize(w)
+    assert rc == 0
+    W_gpu = q4.q4_quantize(torch.from_numpy(w).cuda())
+    assert np.array_equal(W_gpu.cpu().numpy(), W_ref)
+    x = synth.np_activations(1, k, seed=synth.activation_seed(synth.seed_for(1)))
+    Wd, xd = torch.from_numpy(W_ref).cuda(), torch.from_numpy(x).cuda()
+    y = torch.empty((1, n), device="cuda")
+    ws = q4.Workspace()
+    _graph_calls(torch, [lambda s: q4.q4_gemv(Wd, n, k, xd, y=y, workspace=ws,
+                                             flags=q4.FLAG_PDL, stream=s)])
+    Y, S = oracle_mod.matmul(W_ref, n, k, x, nthreads=oracle_mod.cpu_count())
+    ok, info = within_tol(y.cpu().numpy(), Y, S, GEMV_TOL)
+    assert ok, info
+
+
+# --------------------------------------------------------------------- config 2
+
+@pytest.fixture(scope="module")
+def decoder(torch):
+    from bit_weight_quantized_03_b300.stacks import DecoderStack
+    return DecoderStack()
+
+
+MATS = [("wq", "qkv", 0, 4096, 3072, 0), ("wk", "qkv", 4096, 1024, 3072, 1),
+        ("wv", "qkv", 5120, 1024, 3072, 2), ("wo", "wo", 0, 3072, 4096, 3),
+        ("w1", "w13", 0, 9216, 3072, 4), ("w3", "w13", 9216, 9216, 3072, 5),
+        ("w2", "w2", 0, 3072, 9216, 6)]
+
+
+@pytest.mark.parametrize("layer", [0, 13, 25])
+def test_config2_decoder_blocks_match_oracle(torch, oracle_mod, decoder, layer):
+    for name, key, r0, n, k, idx in MATS:
+        rows = _sample_rows(n, 24, seed=layer * 10 + idx)
+        ref = _oracle_rows(oracle_mod, torch, n, k, synth.seed_for(2, layer, idx), rows)
+        got = decoder.W[layer][key][torch.as_tensor(r0 + rows, device="cuda")].cpu().numpy()
+        assert np.array_equal(got, ref), (layer, name)
+
+
+def test_config2_all_104_gemvs_in_bench_launch_config(torch, q4, oracle_mod, decoder):
+    """Every GEMV of a decode step, captured with PDL in one graph as the benchmark
+    runs them, each on its own seeded input; sampled output rows vs the oracle."""
+    outs, ins, calls = [], [], []
+    for l in range(decoder.layers):
+        for key, (n, k) in decoder.shapes.items():
+            x = synth.torch_activations(1, k, seed=synth.activation_seed(synth.seed_for(2, l), 7))
+            y = torch.empty((1, n), device="cuda")
+            W = decoder.W[l][key]
+            calls.append(lambda s, W=W, n=n, k=k, x=x, y=y: q4.q4_gemv(
+                W, n, k, x, y=y, workspace=decoder.ws, flags=q4.FLAG_PDL, stream=s))
+            outs.append((l, key, n, k, y))
+            ins.append(x)
+    _graph_calls(torch, calls)
+    parts = {"qkv": [(4096, 0), (1024, 1), (1024, 2)], "wo": [(3072, 3)],
+             "w13": [(9216, 4), (9216, 5)], "w2": [(3072, 6)]}
+    for (l, key, n, k, y), x in zip(outs, ins):
+        if l not in (0, 7, 25):
+            continue
+        r0 = 0
+        for (pn, idx) in parts[key]:
+            rows = _sample_rows(pn, 12, seed=l + idx)
+            Wr = _oracle_rows(oracle_mod, torch, pn, k, synth.seed_for(2, l, idx), rows)
+            Y, S = oracle_mod.matmul(Wr, len(rows), k, x.cpu().numpy())
+            ok, info = within_tol(y.cpu().numpy()[:, r0 + rows], Y, S, GEMV_TOL)
+            assert ok, (l, key, idx, info)
+            r0 += pn
+
+
+def test_config2_decode_step_exact_properties(torch, decoder):
+    """Full 26-layer step: bit-identical on replay, and exactly scale-equivariant
+    under a power of two (the chain of fp32 GEMVs is linear)."""
+    x0 = synth.torch_activations(1, 3072, seed=synth.activation_seed(2000, 1))
+    s = torch.cuda.Stream()
+    g = decoder.capture([x0], s)
+    g.replay()
+    torch.cuda.synchronize()
+    a = decoder.x.clone()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(a, decoder.x)
+    assert torch.isfinite(a).all()
+    x0.mul_(2.0 ** -10)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(decoder.x, a * 2.0 ** -10)
+
+
+def test_config2_two_layer_chain_vs_oracle_chain(torch, q4, oracle_mod):
+    """Chain wiring: two decoder layers through DecoderStack.step against the
+    oracle applying the same eight products in the same order (fp32 between)."""
+    from bit_weight_quantized_03_b300.stacks import DecoderStack
+    dec = DecoderStack(layers=2)
+    ref = []
+    for l in range(2):
+        mats = {}
+        for key, parts in {"qkv": [(4096, 3072, 0), (1024, 3072, 1), (1024, 3072, 2)],
+                           "wo": [(3072, 4096, 3)],
+                           "w13": [(9216, 3072, 4), (9216, 3072, 5)],
+                           "w2": [(3072, 9216, 6)]}.items():
+            blocks = []
+            for (n, k, idx) in parts:
+                w = synth.torch_weights(n, k, seed=synth.seed_for(2, l, idx)).cpu().numpy()
+                b, rc, _ = oracle_mod.quantize(w)
+                assert rc == 0
+                blocks.append(b)
+            mats[key] = (np.concatenate(blocks), sum(p[0] for p in parts), parts[0][1])
+        ref.append(mats)
+    x0 = synth.torch_activations(1, 3072, seed=synth.activation_seed(2000, 2))
+    dec.step(x0)
+    torch.cuda.synchronize()
+    got = dec.x.cpu().numpy().astype(np.float64)
+    th = oracle_mod.cpu_count()
+    x = x0.cpu().numpy()
+    for l in range(2):
+        W, n, k = ref[l]["qkv"]
+        y, _ = oracle_mod.matmul(W, n, k, x, nthreads=th)
+        W, n, k = ref[l]["wo"]
+        y, _ = oracle_mod.matmul(W, n, k, y[:, :4096].astype(np.float32), nthreads=th)
+        W, n, k = ref[l]["w13"]
+        y, _ = oracle_mod.matmul(W, n, k, y.astype(np.float32), nthreads=th)
+        W, n, k = ref[l]["w2"]
+        y, _ = oracle_mod.matmul(W, n, k, y[:, :9216].astype(np.float32), nthreads=th)
+        x = y.astype(np.float32)
+    rel = np.linalg.norm(got - y) / np.linalg.norm(y)
+    assert rel < 1e-4, rel
+
+
+# --------------------------------------------------------------------- config 3
+
+@pytest.fixture(scope="module")
+def table(torch, q4):
+    V, H, chunk = synth.VOCAB, 3072, 16384
+    T = torch.empty((V, H // 32 * 18), dtype=torch.uint8, device="cuda")
+    for c in range(V // chunk):
+        w = synth.torch_weights(chunk, H, seed=synth.seed_for(3, 0, c))
+        q4.q4_quantize(w, blocks=T[c * chunk:(c + 1) * chunk])
+    torch.cuda.synchronize()
+    return T
+
+
+def _table_rows_ref(oracle_mod, torch, ids):
+    chunk, H = 16384, 3072
+    out = {}
+    for c in sorted(set(int(i) // chunk for i in ids)):
+        w = synth.torch_weights(chunk, H, seed=synth.seed_for(3, 0, c))
+        sel = [int(i) for i in ids if int(i) // chunk == c]
+        rows = w[torch.as_tensor([i - c * chunk for i in sel], device="cuda")].cpu().numpy()
+        b, rc, _ = oracle_mod.quantize(rows)
+        assert rc == 0
+        for j, i in enumerate(sel):
+            out[i] = b[j]
+    return out
+
+
+def test_config3_table_and_gather(torch, q4, oracle_mod, table):
+    V, H = synth.VOCAB, 3072
+    for B in (1, 64, 4096):
+        ids = synth.torch_token_ids(B, V, seed=B)
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        out = torch.empty((B, H), device="cuda")
+        _graph_calls(torch, [lambda s: q4.q4_embed_gather(table, V, H, ids, out=out, status=st,
+                                                          stream=s)])
+        assert int(st.item()) == 0
+        ids_h = ids.cpu().numpy()
+        pick = np.unique(np.concatenate([[0, B - 1], np.random.default_rng(B).integers(0, B, 24)]))
+        ref_blocks = _table_rows_ref(oracle_mod, torch, ids_h[pick])
+        for b in pick:
+            blk = ref_blocks[int(ids_h[b])]
+            assert np.array_equal(table[int(ids_h[b])].cpu().numpy(), blk)
+            assert same_float(out[b].cpu().numpy(), oracle_mod.dequant_rows(blk, 1, H)[0])
+        # every row: the gather equals the decode of the same rows
+        rows = q4.q4_dequant_rows(table, 0, V, H)
+        assert torch.equal(out, rows[ids.long()])
+        del rows
+
+
+def test_config3_head_gemv(torch, q4, oracle_mod, table):
+    V, H = synth.VOCAB, 3072
+    x = synth.torch_activations(1, H, seed=synth.activation_seed(3000))
+    y = torch.empty((1, V), device="cuda")
+    ws = q4.Workspace()
+    _graph_calls(torch, [lambda s: q4.q4_gemv(table, V, H, x, y=y, workspace=ws,
+                                             flags=q4.FLAG_PDL, stream=s)])
+    pick = _sample_rows(V, 200, seed=3)
+    ref = _table_rows_ref(oracle_mod, torch, pick)
+    Wr = np.stack([ref[int(i)] for i in pick])
+    Y, S = oracle_mod.matmul(Wr, len(pick), H, x.cpu().numpy())
+    ok, info = within_tol(y.cpu().numpy()[:, pick], Y, S, GEMV_TOL)
+    assert ok, info
+
+
+# --------------------------------------------------------------------- config 4
+
+@pytest.mark.parametrize("m", synth.ENCODER_FRAMES)
+def test_config4_encoder_gemms(torch, q4, oracle_mod, m):
+    X = synth.torch_activations(m, 1280, seed=synth.activation_seed(4000, m), dtype=torch.bfloat16)
+    for idx, (name, n, k) in enumerate(synth.ENCODER_MATS):
+        w = synth.torch_weights(n, k, seed=synth.seed_for(4, 0, idx))
+        Wg = q4.q4_quantize(w)
+        W_ref, rc, _ = oracle_mod.quantize(w.cpu().numpy())
+        assert rc == 0 and np.array_equal(Wg.cpu().numpy(), W_ref)
+        Xin = X if k == 1280 else synth.torch_activations(
+            m, k, seed=synth.activation_seed(4100, m), dtype=torch.bfloat16)
+        Y = torch.empty((m, n), device="cuda")
+        _graph_calls(torch, [lambda s: q4.q4_gemm(Wg, n, k, Xin, Y=Y, flags=q4.FLAG_PDL,
+                                                  stream=s)])
+        toks = _sample_rows(m, 40, seed=m + idx)
+        Yr, Sr = oracle_mod.matmul(W_ref, n, k, Xin.float().cpu().numpy()[toks],
+                                   nthreads=oracle_mod.cpu_count())
+        ok, info = within_tol(Y.cpu().numpy()[toks], Yr, Sr, GEMM_TOL)
+        assert ok, (name, m, info)
+
+
+# --------------------------------------------------------------------- config 5
+
+@pytest.mark.parametrize("m", [1, 2, 4, 8, 16, 32, 64, 128])
+def test_config5_crossover_shapes(torch, q4, oracle_mod, m):
+    n, k = 4096, 3072
+    w = synth.np_weights(n, k, seed=synth.seed_for(5))
+    W, _, _ = oracle_mod.quantize(w)
+    x = synth.np_activations(m, k, seed=synth.activation_seed(5000, m))
+    Wd = torch.from_numpy(W).cuda()
+    y = q4.q4_linear(Wd, n, k, torch.from_numpy(x).cuda()).cpu().numpy()
+    gemv_path = m <= q4.q4_linear_crossover_m(n, k)
+    Y, S = oracle_mod.matmul(W, n, k, x if gemv_path else bf16_round(x),
+                             nthreads=oracle_mod.cpu_count())
+    ok, info = within_tol(y, Y, S, GEMV_TOL if gemv_path else GEMM_TOL)
+    assert ok, info
+    if m <= q4.GEMV_MAX_M:
+        yv = q4.q4_gemv(Wd, n, k, torch.from_numpy(x).cuda()).cpu().numpy()
+        Y, S = oracle_mod.matmul(W, n, k, x, nthreads=oracle_mod.cpu_count())
+        ok, info = within_tol(yv, Y, S, GEMV_TOL)
+        assert ok, info
+    xb = torch.from_numpy(x).to(torch.bfloat16)
+    yg = q4.q4_gemm(Wd, n, k, xb.cuda()).cpu().numpy()
+    Y, S = oracle_mod.matmul(W, n, k, xb.float().numpy(), nthreads=oracle_mod.cpu_count())
+    ok, info = within_tol(yg, Y, S, GEMM_TOL)
+    assert ok, info
