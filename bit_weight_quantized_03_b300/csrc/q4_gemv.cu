@@ -199,6 +199,7 @@ __global__ void __launch_bounds__(kWarps * 32)
     gemv_stream_kernel(const __grid_constant__ CUtensorMap tmap, const StreamParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t bars[kWarps][kStages];
+  __shared__ __align__(8) uint64_t never[kWarps];  // test hook: nothing ever arrives here
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t wid = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
   if (wid >= p.warps) {
@@ -207,8 +208,10 @@ __global__ void __launch_bounds__(kWarps * 32)
   }
   const uint32_t slots = smem_u32(smem) + warp * (kStages * kSlotBytes);
   const uint32_t bar0 = smem_u32(&bars[warp][0]);
+  const uint32_t never_bar = smem_u32(&never[warp]);
   if (lane == 0) {
     for (int s = 0; s < kStages; ++s) mbar_init(bar0 + 8 * s, 1);
+    mbar_init(never_bar, 1);
     fence_mbarrier_init();
   }
   __syncwarp();
@@ -225,9 +228,7 @@ __global__ void __launch_bounds__(kWarps * 32)
       const int64_t g = u / p.nsb, sb = u - g * p.nsb;
       const int slot = static_cast<int>((u - u0) % kStages);
       const uint32_t bar = bar0 + 8 * slot;
-      uint32_t bytes = kSlotBytes;
-      if (stall_test && u == u0) bytes += 16;  // test hook: this phase never completes
-      mbar_arrive_expect_tx(bar, bytes);
+      mbar_arrive_expect_tx(bar, kSlotBytes);
       tma_load_2d_hint(slots + slot * kSlotBytes, &tmap, static_cast<int32_t>(sb * kSuperBytes),
                        static_cast<int32_t>(g * 32), bar, pol);
     }
@@ -249,8 +250,11 @@ __global__ void __launch_bounds__(kWarps * 32)
   for (; u < u1; ++u) {
     const int slot = static_cast<int>((u - u0) % kStages);
     const uint32_t parity = static_cast<uint32_t>(((u - u0) / kStages) & 1);
-    // every lane waits; the verdict is made warp-uniform before any __syncwarp
-    const bool landed = mbar_wait(bar0 + 8 * slot, parity);
+    // every lane waits; the verdict is made warp-uniform before any __syncwarp.
+    // The test hook waits on a barrier that nothing arrives on, so that wait
+    // runs out after kWaitLimitNs.
+    const bool landed = (stall_test && u == u0) ? mbar_wait(never_bar, 0)
+                                                 : mbar_wait(bar0 + 8 * slot, parity);
     if (!__all_sync(0xffffffffu, landed)) {
       ok = false;
       break;
@@ -335,8 +339,9 @@ __global__ void __launch_bounds__(kWarps * 32)
 
   if (!ok) {
     if (lane == 0) report(p.status, 6 /* Q4_ERR_TIMEOUT */);
-    // Let every copy this warp still has in flight land before the CTA exits.
-    for (int64_t v = u + 1; v < issued; ++v) {
+    // Let every copy this warp still has in flight (unit u's included) land
+    // before the CTA exits; each of these waits is bounded too.
+    for (int64_t v = u; v < issued; ++v) {
       const int slot = static_cast<int>((v - u0) % kStages);
       const uint32_t parity = static_cast<uint32_t>(((v - u0) / kStages) & 1);
       mbar_wait(bar0 + 8 * slot, parity);
