@@ -17,10 +17,11 @@ from __future__ import annotations
 from ._lib import (BF16, BLOCK_BYTES, BLOCK_ELEMS, ERR_CUDA, ERR_ID_OUT_OF_RANGE,  # noqa: F401
                    ERR_INVALID_ARG, ERR_MISALIGNED, ERR_NONFINITE, ERR_TIMEOUT,
                    ERR_UNSUPPORTED_SHAPE, ERR_WORKSPACE, F32, FLAG_PDL, FLAG_TEST_STALL,
-                   GEMV_MAX_M, OK, Q4Error, check, lib, status_string)
+                   GEMV_MAX_M, GEMV_NOALLOC_SCRATCH_BYTES, OK, Q4Error, check, lib,
+                   status_string)
 
 __all__ = [
-    "q4_quantize", "q4_dequant_rows", "q4_gemv", "q4_gemm", "q4_embed_gather", "q4_linear",
+    "q4_quantize", "q4_dequant_rows", "q4_gemv", "q4_gemv_noalloc", "q4_gemm", "q4_embed_gather", "q4_linear",
     "q4_gemv_workspace_bytes", "q4_gemm_workspace_bytes", "q4_linear_workspace_bytes",
     "q4_linear_crossover_m", "Workspace", "Q4Error", "lib", "packed_bytes",
 ]
@@ -147,6 +148,22 @@ def q4_gemv(W, n: int, k: int, x, y=None, workspace=None, status=None, flags: in
     buf, nbytes = _workspace(workspace, q4_gemv_workspace_bytes(n, k, m))
     check(lib().q4_gemv(_ptr(W), n, k, _ptr(x), m, ldx, _ptr(y), ldy, _ptr(buf), nbytes,
                         _ptr(status), flags, _stream(stream)), "q4_gemv")
+    return y
+
+
+def q4_gemv_noalloc(W, n: int, k: int, x, y=None, status=None, flags: int = 0, stream=None):
+    """q4_gemv for callers that cannot allocate device memory: no workspace
+    argument; the split-K scratch is a fixed array inside the library (the
+    output y is allocated here only when the caller passes none).  Calls that
+    may overlap on the GPU share that array and race: keep them on one stream."""
+    torch = _torch()
+    m = x.shape[0]
+    ldx = _row_stride(x, "x")
+    if y is None:
+        y = torch.empty((m, n), dtype=torch.float32, device=x.device)
+    ldy = _row_stride(y, "y")
+    check(lib().q4_gemv_noalloc(_ptr(W), n, k, _ptr(x), m, ldx, _ptr(y), ldy, _ptr(status),
+                                flags, _stream(stream)), "q4_gemv_noalloc")
     return y
 
 

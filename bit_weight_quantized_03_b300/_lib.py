@@ -25,6 +25,7 @@ BF16 = 1
 FLAG_PDL = 1
 FLAG_TEST_STALL = 1 << 30
 GEMV_MAX_M = 16
+GEMV_NOALLOC_SCRATCH_BYTES = 4 << 20
 BLOCK_ELEMS = 32
 BLOCK_BYTES = 18
 
@@ -36,6 +37,7 @@ SIGNATURES = {
     "q4_dequant_rows": (_st, [_vp, _i64, _i64, _i64, _vp, ctypes.c_int, _vp]),
     "q4_gemv": (_st, [_vp, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _vp, _sz, _vp, _u32, _vp]),
     "q4_gemv_workspace_bytes": (_sz, [_i64, _i64, _i64]),
+    "q4_gemv_noalloc": (_st, [_vp, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _vp, _u32, _vp]),
     "q4_gemm": (_st, [_vp, _i64, _i64, _vp, _i64, _i64, _vp, ctypes.c_int, _i64, _vp, _sz, _vp,
                       _u32, _vp]),
     "q4_gemm_workspace_bytes": (_sz, [_i64, _i64, _i64]),

@@ -119,6 +119,28 @@ q4_status q4_gemv(const void* W, int64_t n, int64_t k, const float* x, int64_t m
                   uint32_t flags, q4_stream_t s);
 size_t q4_gemv_workspace_bytes(int64_t n, int64_t k, int64_t m);
 
+/* q4_gemv for callers that cannot allocate device memory (a host that embeds
+ * the library in a fixed memory pool where cudaMalloc is forbidden, a
+ * real-time loop that must not allocate once streaming has started, a plugin
+ * that is handed only its input and output buffers).  The pages have no
+ * counterpart: it is a packaging choice of this library.
+ * Same arguments, result and error behaviour as q4_gemv, minus the workspace:
+ * the split-K scratch is one array of Q4_GEMV_NOALLOC_SCRATCH_BYTES inside the
+ * library, in device memory of every GPU that loads it, held until exit.  A
+ * call whose q4_gemv_workspace_bytes(n, k, m) exceeds that size returns
+ * Q4_ERR_UNSUPPORTED_SHAPE and launches nothing (on a 148-SM B300 every
+ * m <= 8 with n <= 2^20 fits).  The call allocates nothing; it clears the
+ * part of the array it uses on stream `s` (cudaMemsetAsync) and then runs
+ * the q4_gemv kernels.  The first call on each device looks up the array's
+ * device address with that device current: make it before any stream
+ * capture.  All calls share the array, so calls that may overlap on the GPU
+ * (other streams, other host threads) race and give wrong results; serialise
+ * them on one stream. */
+#define Q4_GEMV_NOALLOC_SCRATCH_BYTES 4194304 /* 4 MiB */
+q4_status q4_gemv_noalloc(const void* W, int64_t n, int64_t k, const float* x, int64_t m,
+                          int64_t ldx, float* y, int64_t ldy, int32_t* status_dev,
+                          uint32_t flags, q4_stream_t s);
+
 /* Prefill / audio-encoder product on the tensor cores:
  *   Y[i][r] = sum_j bf16(w^[r][j]) * X[i][j]   (fp32 accumulation)
  * for the 32-layer, 1280-wide encoder and prefill ("Arquitectura"); error within
