@@ -224,10 +224,7 @@ def _time_graph_replays(graphs, stream, torch):
 def run_ours(args):
     import torch
 
-    import synth
-    from bit_weight_quantized_03_b300 import (FLAG_PDL, Workspace, lib, q4_embed_gather,
-                                              q4_gemv, q4_quantize)
-    from bit_weight_quantized_03_b300.stacks import DecoderStack, EncoderStack
+    from bit_weight_quantized_03_b300 import lib
 
     world, rank, local = _dist()
     if world > 1:
@@ -240,6 +237,38 @@ def run_ours(args):
     hbm, bf16_burst, bf16_sust, peak_src = _peaks()
     dev = torch.device("cuda", torch.cuda.current_device())
     stream = torch.cuda.Stream()
+
+    line = {
+        "metric": METRIC, "value": None, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": None,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp32",
+        "data": "synthetic (seeded N(0,0.02^2) weights quantized on device, N(0,1) activations)",
+    }
+    if args.only in ("all", "stack"):
+        line.update(_run_stack(args, world, dev, stream, hbm, peak_src, torch))
+    extra = {}
+    if args.only in ("all", "head", "gather"):
+        extra = _run_head_gather(args, dev, stream, hbm, torch)
+    gemm = None
+    if args.only in ("all", "gemm"):
+        gemm = _run_gemm(args, world, dev, stream, bf16_burst, bf16_sust, peak_src, torch)
+    cpu = None
+    if rank == 0 and world == 1 and args.cpu_seconds > 0:
+        cpu = _oracle_sample(seconds=args.cpu_seconds)
+    line["cpu_baseline"] = cpu
+    line["prefill_gemm"] = gemm
+    line.update(extra)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def _run_stack(args, world, dev, stream, hbm, peak_src, torch):
+    import synth
+    from bit_weight_quantized_03_b300.stacks import DecoderStack
 
     # ---------------- decoder stack (headline)
     dec = DecoderStack(device=dev)
@@ -293,10 +322,33 @@ def run_ours(args):
            "h2d_bytes_per_step": 3072 * 4, "d2h_bytes_per_step": 3072 * 4,
            "ms_per_step": e2e_s / args.steps * 1e3}
     del g_e2e
+    return {
+        "value": value, "ms_per_step": ms_step,
+        "config": {"workload": WORKLOAD, "layers": dec.layers, "hidden": 3072,
+                   "gqa": "32Q/8KV", "ffn": 9216, "batch": 1,
+                   "weight_bytes_per_step": wbytes, "activation_bytes_per_step": abytes,
+                   "l2": "inputs larger than L2: 1.70 GB of weights per step vs 126 MB L2",
+                   "graph": f"CUDA graphs of {G} steps (PDL between the 104 GEMVs of a step)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "traffic": args.traffic,
+                     "kernel": "gemv_stream_kernel<1>",
+                     "peak_source": f"{peak_src} HBM copy bandwidth",
+                     "per_launch": "algorithmic bytes of the 104 launches of a step / step time"},
+        "e2e": e2e,
+        "gpu_launches": dec.launches_per_step() * args.steps,
+        "clocks": clocks,
+    }
+
+
+def _run_head_gather(args, dev, stream, hbm, torch):
+    import synth
+    from bit_weight_quantized_03_b300 import FLAG_PDL, Workspace, q4_embed_gather, q4_gemv, \
+        q4_quantize
 
     # ---------------- output head GEMV and embedding gather (131072 x 3072 table)
     extra = {}
-    if not args.skip_extra:
+    if True:
         V, H = synth.VOCAB, 3072
         table = torch.empty((V, H // 32 * 18), dtype=torch.uint8, device=dev)
         for r0 in range(0, V, 16384):
@@ -341,10 +393,16 @@ def run_ours(args):
             gather[str(B)] = {"us_per_call": gms * 1e3, "gbs": nbytes / (gms * 1e-3) / 1e9}
         extra["embed_gather"] = gather
         del table, gh
+    return extra
+
+
+def _run_gemm(args, world, dev, stream, bf16_burst, bf16_sust, peak_src, torch):
+    import synth
+    from bit_weight_quantized_03_b300.stacks import EncoderStack
 
     # ---------------- prefill / encoder GEMM
     gemm = None
-    if not args.skip_gemm:
+    if True:
         M = 3000
         try:
             enc = EncoderStack(frames=M, device=dev)
@@ -366,38 +424,7 @@ def run_ours(args):
             del enc, ge
         except Exception as e:  # reported, never silently replaced
             gemm = {"error": f"{type(e).__name__}: {e}"}
-
-    cpu = _oracle_sample(seconds=args.cpu_seconds) if rank == 0 and world == 1 else None
-
-    line = {
-        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp32",
-        "data": "synthetic (seeded N(0,0.02^2) weights quantized on device, N(0,1) activations)",
-        "config": {"workload": WORKLOAD, "layers": dec.layers, "hidden": 3072,
-                   "gqa": "32Q/8KV", "ffn": 9216, "batch": 1,
-                   "weight_bytes_per_step": wbytes, "activation_bytes_per_step": abytes,
-                   "l2": "inputs larger than L2: 1.70 GB of weights per step vs 126 MB L2",
-                   "graph": f"CUDA graphs of {G} steps (PDL between the 104 GEMVs of a step)",
-                   "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "traffic": args.traffic,
-                     "kernel": "gemv_stream_kernel<1>",
-                     "peak_source": f"{peak_src} HBM copy bandwidth",
-                     "per_launch": "algorithmic bytes of the 104 launches of a step / step time"},
-        "cpu_baseline": cpu,
-        "e2e": e2e,
-        "gpu_launches": dec.launches_per_step() * args.steps,
-        "clocks": clocks,
-        "prefill_gemm": gemm,
-    }
-    line.update(extra)
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
-    return 0
+    return gemm
 
 
 def main():
@@ -406,8 +433,8 @@ def main():
     ap.add_argument("--steps", type=int, default=256)
     ap.add_argument("--warmup", type=int, default=16)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--skip-gemm", action="store_true")
-    ap.add_argument("--skip-extra", action="store_true")
+    ap.add_argument("--only", choices=["all", "stack", "head", "gather", "gemm"], default="all",
+                    help="run one section (profiling runs); the default runs all of them")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--traffic", type=float, default=None,
                     help="per-launch DRAM bytes of the GEMV kernel from an ncu capture")
