@@ -427,8 +427,9 @@ GemvPlan gemv_plan(int64_t n, int64_t k, int64_t m) {
   p.groups = (n + 31) / 32;
   if (!p.fast) return p;
   p.units = p.groups * (k / kSuperElems);
+  p.b1 = (m == 1);
   const int64_t target = static_cast<int64_t>(sm_count()) * kCtasPerSm * kWarps;
-  p.warps = p.units < target ? p.units : target;
+  p.warps = p.b1 ? gemv_b1_warps(p.units) : (p.units < target ? p.units : target);
   const size_t cnt_bytes = (static_cast<size_t>(p.groups) * 4 + 255) / 256 * 256;
   p.ws_bytes = cnt_bytes + static_cast<size_t>(p.warps) * 2 * static_cast<size_t>(m) * 32 * 4;
   return p;
@@ -438,6 +439,12 @@ cudaError_t gemv_launch(const GemvPlan& plan, const uint8_t* W, int64_t n, int64
                         const float* x, int64_t m, int64_t ldx, float* y, int64_t ldy,
                         void* workspace, int32_t* status, uint32_t flags, cudaStream_t s) {
   const bool pdl = (flags & 1u) != 0;
+  if (plan.fast && plan.b1 && m == 1) {
+    const size_t cnt_bytes = (static_cast<size_t>(plan.groups) * 4 + 255) / 256 * 256;
+    return gemv_b1_launch(W, n, k, x, y, static_cast<int32_t*>(workspace),
+                          reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + cnt_bytes),
+                          plan.units, plan.warps, status, flags, s);
+  }
   switch (m) {
 #define Q4_GEMV_CASE(MM) \
   case MM:               \

@@ -1,0 +1,422 @@
+// q4_gemv_b1.cu -- fused Q4_0 dequant-GEMV at batch 1 (one token per decode step):
+//   y[r] = sum_j ((q[r][j] - 8) * d[r][j/32]) * x[j],  fp32 accumulation.
+//
+// This is the per-token product of every decoder linear and of the output head
+// in the Voxtral Mini 4B Realtime port (GeekNews, es.news.hada.io/topic?id=26595,
+// "Arquitectura": 26-layer decoder, hidden 3072, GQA 32Q/8KV, GGUF Q4_0
+// weights through custom GPU shaders).  Each weight is read once and used
+// once, so the kernel has to decode Q4_0 as fast as HBM delivers it: at the
+// measured ~6.5 TB/s that is ~38 weights per SM clock, against an integer ALU
+// pipe that retires 64 lane-operations per SM clock.  The design therefore
+// spends one ALU operation per weight and keeps everything else on the FMA
+// pipe or out of the loop:
+//
+//   * Work unit = 32 rows x 256 weights (8 blocks = 144 contiguous bytes per
+//     row).  Units are ordered row-group major; every warp takes one contiguous
+//     range of them ("stream-K"), so each warp gets the same number +-1.
+//   * Each warp streams its units through its own ring of shared-memory slots,
+//     one 2-D TMA tile (144 B x 32 rows, evict-first) per unit.  The ring is
+//     filled before waiting on the previous kernel (programmatic dependent
+//     launch), so weight reads overlap the previous layer's tail.
+//   * Lane l works on block pair j = l % 4 (weights 64j .. 64j+63 of the unit)
+//     of rows l/4, l/4 + 8, l/4 + 16, l/4 + 24.  Its 64 activations are loaded
+//     once per unit into registers as fp32 pairs and serve all four rows; the
+//     36 bytes of a block pair start on a 4-byte boundary, and the lanes' 32-bit
+//     shared loads hit 32 distinct banks.
+//   * Decode: a nibble at bit p <= 16 of a 32-bit word becomes the float
+//     2^(23-p) + q with one AND/OR (LOP3, the one ALU operation per weight);
+//     the nibbles at bits 20..31 are first moved down by 12 bits with an
+//     integer multiply-high (FMA pipe).  One packed fp32x2 subtract gives
+//     (q - 8) exactly for two weights, one packed fp32x2 FMA multiplies them by
+//     the adjacent activation pair.  Per block the 32 products are summed and
+//     scaled by d once.
+//   * Row groups split between warps are finished deterministically: partial
+//     row sums go to the workspace, the last warp to arrive (atomic counter)
+//     adds them in warp order, zeroes them and resets the counter.
+#include "q4_device.cuh"
+
+namespace q4 {
+namespace {
+
+constexpr int kWarps = 4;                     // warps per CTA
+constexpr int kStages = 3;                    // ring slots per warp
+constexpr int kCtasPerSm = 4;                 // 16 warps per SM
+constexpr int kSlotBytes = 32 * kSuperBytes;  // 32 rows x 144 B
+constexpr int kSmemBytes = kWarps * kStages * kSlotBytes;
+
+struct B1Params {
+  const uint8_t* W;
+  int64_t n, nsb;
+  const float* x;
+  float* y;
+  int32_t* counters;  // [groups]
+  float* partials;    // [warps][2][32]
+  int64_t units, warps;
+  int32_t* status;
+  uint32_t flags;
+};
+
+// w >> 12 computed as the high word of w * 2^20: an integer multiply, issued
+// to the FMA pipe instead of the (busier) ALU pipe.
+__device__ __forceinline__ uint32_t shr12(uint32_t w) { return __umulhi(w, 1u << 20); }
+
+// Loop-invariant decode constants, kept in registers: the exponent bits of
+// 2^(23-p) for the five nibble positions p = 0, 4, 8, 12, 16, and the packed
+// (2^(23-pa) + 8, 2^(23-pb) + 8) bias pairs of the four position pairs used.
+// Written through an opaque move so that each magic OR stays one LOP3 (mask as
+// the immediate, bits from the register) instead of an AND plus an OR.
+struct DecodeConsts {
+  uint32_t bits[5];
+  unsigned long long bias_16_12, bias_8_16, bias_0_8, bias_4_12;
+};
+
+__device__ __forceinline__ uint32_t opaque(uint32_t v) {
+  uint32_t r;
+  asm volatile("mov.b32 %0, %1;" : "=r"(r) : "r"(v));
+  return r;
+}
+
+__device__ __forceinline__ DecodeConsts make_consts() {
+  DecodeConsts c;
+  c.bits[0] = opaque(NibbleMagic<0>::kBits);
+  c.bits[1] = opaque(NibbleMagic<4>::kBits);
+  c.bits[2] = opaque(NibbleMagic<8>::kBits);
+  c.bits[3] = opaque(NibbleMagic<12>::kBits);
+  c.bits[4] = opaque(NibbleMagic<16>::kBits);
+  auto bias = [](float a, float b) {
+    return pack2(__uint_as_float(opaque(__float_as_uint(a))),
+                 __uint_as_float(opaque(__float_as_uint(b))));
+  };
+  c.bias_16_12 = bias(NibbleMagic<16>::kBias, NibbleMagic<12>::kBias);
+  c.bias_8_16 = bias(NibbleMagic<8>::kBias, NibbleMagic<16>::kBias);
+  c.bias_0_8 = bias(NibbleMagic<0>::kBias, NibbleMagic<8>::kBias);
+  c.bias_4_12 = bias(NibbleMagic<4>::kBias, NibbleMagic<12>::kBias);
+  return c;
+}
+
+template <int P>
+__device__ __forceinline__ uint32_t pos_bits(const DecodeConsts& c) {
+  return c.bits[P / 4];
+}
+
+template <int PA, int PB>
+__device__ __forceinline__ unsigned long long pair_bias(const DecodeConsts& c) {
+  if constexpr (PA == 16 && PB == 12) return c.bias_16_12;
+  else if constexpr (PA == 8 && PB == 16) return c.bias_8_16;
+  else if constexpr (PA == 0 && PB == 8) return c.bias_0_8;
+  else return c.bias_4_12;
+}
+
+// (q - 8) for the weight pair whose nibbles sit at bit PA of wa and PB of wb:
+// two LOP3 ((w & 0xF << p) | bits(2^(23-p))) and one packed fp32x2 subtract.
+template <int PA, int PB>
+__device__ __forceinline__ unsigned long long qm8(uint32_t wa, uint32_t wb,
+                                                  const DecodeConsts& c) {
+  static_assert((PA == 16 && PB == 12) || (PA == 8 && PB == 16) || (PA == 0 && PB == 8) ||
+                    (PA == 4 && PB == 12),
+                "position pair without a bias constant");
+  unsigned long long r;
+  asm("{\n\t.reg .b32 lo, hi;\n\t"
+      "lop3.b32 lo, %1, %3, %4, 0xEA;\n\t"
+      "lop3.b32 hi, %2, %5, %6, 0xEA;\n\t"
+      "mov.b64 %0, {lo, hi};\n\t"
+      "sub.rn.f32x2 %0, %0, %7;\n\t}"
+      : "=l"(r)
+      : "r"(wa), "r"(wb), "n"(NibbleMagic<PA>::kMask), "r"(pos_bits<PA>(c)),
+        "n"(NibbleMagic<PB>::kMask), "r"(pos_bits<PB>(c)), "l"(pair_bias<PA, PB>(c)));
+  return r;
+}
+
+// Dot product of block BLK (0 or 1) of a 36-byte block pair r[9] with the
+// activation pairs xp[16 * BLK ..]: returns sum_e (q_e - 8) * x_e as an fp32
+// pair (even and odd elements) and the block's scale in d.
+//   BLK 0: d = low half of r[0]; qs[0..1] high half of r[0], qs[2..13] in
+//          r[1..3], qs[14..15] low half of r[4].
+//   BLK 1: d = high half of r[4]; qs[0..15] in r[5..8].
+// Byte c of qs holds element c (low nibble) and element c + 16 (high nibble).
+template <int BLK>
+__device__ __forceinline__ unsigned long long block_dot(const uint32_t (&r)[9],
+                                                        const unsigned long long (&xp)[32],
+                                                        const DecodeConsts& c, float& d) {
+  const unsigned long long* xb = xp + 16 * BLK;
+  unsigned long long acc;
+  if constexpr (BLK == 0) {
+    d = half_bits_to_float(r[0]);
+    {
+      const uint32_t w = r[0], t = shr12(w);
+      acc = fmul2(qm8<16, 12>(w, t, c), xb[0]);          // elements 0, 1
+      acc = ffma2(qm8<8, 16>(t, t, c), xb[8], acc);      // 16, 17
+    }
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+      const uint32_t w = r[1 + i], t = shr12(w);      // qs[2+4i .. 5+4i]
+      acc = ffma2(qm8<0, 8>(w, w, c), xb[1 + 2 * i], acc);    // 2+4i, 3+4i
+      acc = ffma2(qm8<16, 12>(w, t, c), xb[2 + 2 * i], acc);  // 4+4i, 5+4i
+      acc = ffma2(qm8<4, 12>(w, w, c), xb[9 + 2 * i], acc);   // 18+4i, 19+4i
+      acc = ffma2(qm8<8, 16>(t, t, c), xb[10 + 2 * i], acc);  // 20+4i, 21+4i
+    }
+    {
+      const uint32_t w = r[4];
+      acc = ffma2(qm8<0, 8>(w, w, c), xb[7], acc);   // 14, 15
+      acc = ffma2(qm8<4, 12>(w, w, c), xb[15], acc); // 30, 31
+    }
+  } else {
+    d = half_bits_to_float(r[4] >> 16);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t w = r[5 + i], t = shr12(w);      // qs[4i .. 4i+3]
+      const unsigned long long a = qm8<0, 8>(w, w, c);   // 4i, 4i+1
+      acc = i == 0 ? fmul2(a, xb[0]) : ffma2(a, xb[2 * i], acc);
+      acc = ffma2(qm8<16, 12>(w, t, c), xb[2 * i + 1], acc);  // 4i+2, 4i+3
+      acc = ffma2(qm8<4, 12>(w, w, c), xb[8 + 2 * i], acc);   // 4i+16, 4i+17
+      acc = ffma2(qm8<8, 16>(t, t, c), xb[9 + 2 * i], acc);   // 4i+18, 4i+19
+    }
+  }
+  return acc;
+}
+
+__device__ __forceinline__ void ldg_nc_v2u64(const void* p, unsigned long long& a,
+                                             unsigned long long& b) {
+  asm volatile("ld.global.nc.v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p));
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+
+// First unit of warp i when `units` units are cut into `warps` contiguous
+// ranges [units*i/warps, units*(i+1)/warps), and the warp that owns unit u.
+__device__ __forceinline__ int64_t range_start(int64_t i, int64_t units, int64_t warps) {
+  return units * i / warps;
+}
+__device__ __forceinline__ int64_t owner_of(int64_t u, int64_t units, int64_t warps) {
+  return ((u + 1) * warps - 1) / units;
+}
+
+__global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
+    gemv_b1_kernel(const __grid_constant__ CUtensorMap tmap, const B1Params p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t bars[kWarps][kStages];
+  __shared__ __align__(8) uint64_t never[kWarps];  // test hook: nothing ever arrives here
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t wid = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
+  if (wid >= p.warps) {
+    pdl_allow_dependents();
+    return;
+  }
+  const uint32_t slots = smem_u32(smem) + warp * (kStages * kSlotBytes);
+  const uint32_t bar0 = smem_u32(&bars[warp][0]);
+  const uint32_t never_bar = smem_u32(&never[warp]);
+  if (lane == 0) {
+    for (int s = 0; s < kStages; ++s) mbar_init(bar0 + 8 * s, 1);
+    mbar_init(never_bar, 1);
+    fence_mbarrier_init();
+  }
+  __syncwarp();
+
+  const int64_t u0 = range_start(wid, p.units, p.warps);
+  const int64_t nunits = range_start(wid + 1, p.units, p.warps) - u0;  // >= 1
+  const uint64_t pol = l2_evict_first_policy();
+  const bool stall_test = (p.flags & kFlagTestStallOneWait) != 0 && wid == 0;
+  const int64_t g_first = u0 / p.nsb;
+
+  // Producer side: the next unit to load, walked without divisions.
+  int64_t ig = g_first, isb = u0 - g_first * p.nsb, issued = 0;
+  int islot = 0;
+  auto issue_next = [&]() {
+    if (lane == 0) {
+      const uint32_t bar = bar0 + 8 * islot;
+      mbar_arrive_expect_tx(bar, kSlotBytes);
+      tma_load_2d_hint(slots + islot * kSlotBytes, &tmap, static_cast<int32_t>(isb * kSuperBytes),
+                       static_cast<int32_t>(ig * 32), bar, pol);
+    }
+    ++issued;
+    if (++isb == p.nsb) {
+      isb = 0;
+      ++ig;
+    }
+    if (++islot == kStages) islot = 0;
+  };
+  while (issued < nunits && issued < kStages) issue_next();
+
+  pdl_allow_dependents();
+  pdl_wait_prior_grid();  // x, y and the workspace are now safe to touch
+
+  const DecodeConsts dc = make_consts();
+  const int j = lane & 3;    // block pair within the unit
+  const int rr = lane >> 2;  // rows rr, rr + 8, rr + 16, rr + 24 of the group
+  float yv[4] = {0.f, 0.f, 0.f, 0.f};
+
+  // Consumer side: unit `done` of the range is (g, sb) in ring slot `slot`.
+  int64_t g = g_first, sb = u0 - g_first * p.nsb, done = 0;
+  int slot = 0;
+  uint32_t parity = 0;
+  bool ok = true;
+  for (; done < nunits; ++done) {
+    unsigned long long xp[32];
+    {
+      const float* xs = p.x + sb * kSuperElems + 64 * j;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) ldg_nc_v2u64(xs + 4 * i, xp[2 * i], xp[2 * i + 1]);
+    }
+    // every lane waits; the verdict is made warp-uniform before any __syncwarp.
+    // The test hook waits on a barrier that nothing arrives on, so that wait
+    // runs out after kWaitLimitNs.
+    const bool landed = (stall_test && done == 0) ? mbar_wait(never_bar, 0)
+                                                   : mbar_wait(bar0 + 8 * slot, parity);
+    if (!__all_sync(0xffffffffu, landed)) {
+      ok = false;
+      break;
+    }
+    const uint32_t src = slots + slot * kSlotBytes + rr * kSuperBytes + 36 * j;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint32_t r[9];
+#pragma unroll
+      for (int w = 0; w < 9; ++w) r[w] = lds32(src + i * 8 * kSuperBytes + 4 * w);
+      float d0, d1;
+      const f2 a0 = unpack2(block_dot<0>(r, xp, dc, d0));
+      const f2 a1 = unpack2(block_dot<1>(r, xp, dc, d1));
+      yv[i] = fmaf(a0.x + a0.y, d0, yv[i]);
+      yv[i] = fmaf(a1.x + a1.y, d1, yv[i]);
+    }
+    __syncwarp();
+    fence_proxy_async_smem();
+    if (issued < nunits) issue_next();
+
+    if (sb == p.nsb - 1 || done == nunits - 1) {
+      // Row group g is done for this warp: the four lanes of a quad hold the
+      // four block-pair sums of the same rows; add them (fixed order).
+      float v[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        v[i] = yv[i];
+        v[i] += __shfl_xor_sync(0xffffffffu, v[i], 1);
+        v[i] += __shfl_xor_sync(0xffffffffu, v[i], 2);
+        yv[i] = 0.f;
+      }
+      const int64_t gu0 = g * p.nsb, gu1 = gu0 + p.nsb;
+      if (gu0 >= u0 && gu1 <= u0 + nunits) {
+        if (j == 0) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int64_t row = g * 32 + rr + 8 * i;
+            if (row < p.n) p.y[row] = v[i];
+          }
+        }
+      } else {
+        // Partial slot 0 holds a warp's first row group, slot 1 its last.
+        float* mine = p.partials + (wid * 2 + (g == g_first ? 0 : 1)) * 32;
+        if (j == 0) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) __stcg(mine + rr + 8 * i, v[i]);
+        }
+        __threadfence();
+        __syncwarp();
+        const int64_t i0 = owner_of(gu0, p.units, p.warps);
+        const int64_t i1 = owner_of(gu1 - 1, p.units, p.warps);
+        int last = 0;
+        if (lane == 0) last = atomicAdd(&p.counters[g], 1) == static_cast<int>(i1 - i0);
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last) {
+          __threadfence();
+          // Owner i0 may have started in an earlier group (then this group is
+          // its slot 1); every later owner starts inside this group (slot 0).
+          const int64_t i0_slot = range_start(i0, p.units, p.warps) < gu0 ? 1 : 0;
+          const int np = static_cast<int>(i1 - i0 + 1);
+          float s = 0.f;
+          for (int b = 0; b < np; b += 8) {
+            float pv[8];
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+              const int64_t i = i0 + b + t;
+              const int64_t sl = (t == 0 && b == 0) ? i0_slot : 0;
+              pv[t] = (b + t < np) ? __ldcg(p.partials + (i * 2 + sl) * 32 + lane) : 0.f;
+            }
+#pragma unroll
+            for (int t = 0; t < 8; ++t)
+              if (b + t < np) s += pv[t];  // warp order: deterministic
+          }
+          for (int b = 0; b < np; ++b) {  // the workspace goes back to all-zero
+            const int64_t sl = b == 0 ? i0_slot : 0;
+            __stcg(p.partials + ((i0 + b) * 2 + sl) * 32 + lane, 0.f);
+          }
+          const int64_t row = g * 32 + lane;
+          if (row < p.n) p.y[row] = s;
+          if (lane == 0) p.counters[g] = 0;
+        }
+      }
+    }
+    if (++sb == p.nsb) {
+      sb = 0;
+      ++g;
+    }
+    if (++slot == kStages) {
+      slot = 0;
+      parity ^= 1u;
+    }
+  }
+
+  if (!ok) {
+    if (lane == 0) report(p.status, 6 /* Q4_ERR_TIMEOUT */);
+    // Let every copy this warp still has in flight (unit `done`'s included)
+    // land before the CTA exits; each of these waits is bounded too.
+    for (int64_t v = done; v < issued; ++v)
+      mbar_wait(bar0 + 8 * static_cast<uint32_t>(v % kStages),
+                static_cast<uint32_t>((v / kStages) & 1));
+  }
+}
+
+}  // namespace
+
+int64_t gemv_b1_warps(int64_t units) {
+  const int64_t target = static_cast<int64_t>(sm_count()) * kCtasPerSm * kWarps;
+  return units < target ? units : target;
+}
+
+cudaError_t gemv_b1_launch(const uint8_t* W, int64_t n, int64_t k, const float* x, float* y,
+                           int32_t* counters, float* partials, int64_t units, int64_t warps,
+                           int32_t* status, uint32_t flags, cudaStream_t s) {
+  const int64_t rowbytes = k / 32 * kBlockBytes;
+  CUtensorMap tmap;
+  if (!encode_tmap_2d(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, static_cast<uint64_t>(rowbytes),
+                      static_cast<uint64_t>(n), static_cast<uint64_t>(rowbytes), kSuperBytes, 32,
+                      CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
+  static bool configured[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(gemv_b1_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  B1Params p;
+  p.W = W;
+  p.n = n;
+  p.nsb = k / kSuperElems;
+  p.x = x;
+  p.y = y;
+  p.counters = counters;
+  p.partials = partials;
+  p.units = units;
+  p.warps = warps;
+  p.status = status;
+  p.flags = flags;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((warps + kWarps - 1) / kWarps));
+  cfg.blockDim = dim3(kWarps * 32);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = (flags & 1u) ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, gemv_b1_kernel, tmap, p);
+}
+
+}  // namespace q4
