@@ -427,7 +427,7 @@ GemvPlan gemv_plan(int64_t n, int64_t k, int64_t m) {
   p.groups = (n + 31) / 32;
   if (!p.fast) return p;
   p.units = p.groups * (k / kSuperElems);
-  p.b1 = (m == 1);
+  p.b1 = (m == 1) && gemv_b1_supports(k);
   const int64_t target = static_cast<int64_t>(sm_count()) * kCtasPerSm * kWarps;
   p.warps = p.b1 ? gemv_b1_warps(p.units) : (p.units < target ? p.units : target);
   const size_t cnt_bytes = (static_cast<size_t>(p.groups) * 4 + 255) / 256 * 256;

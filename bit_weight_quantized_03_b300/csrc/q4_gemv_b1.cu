@@ -38,11 +38,17 @@
 namespace q4 {
 namespace {
 
-constexpr int kWarps = 4;                     // warps per CTA
-constexpr int kStages = 3;                    // ring slots per warp
-constexpr int kCtasPerSm = 4;                 // 16 warps per SM
+constexpr int kWarps = 16;                    // warps per CTA, one CTA per SM
+constexpr int kStages = 2;                    // ring slots per warp
 constexpr int kSlotBytes = 32 * kSuperBytes;  // 32 rows x 144 B
-constexpr int kSmemBytes = kWarps * kStages * kSlotBytes;
+constexpr int kRingBytes = kWarps * kStages * kSlotBytes;
+constexpr int kMaxSmem = 226 * 1024;  // dynamic part; the static barriers need the rest
+
+// x is staged once per CTA in shared memory, with 16 bytes of padding after
+// every 64 floats, so that the four block pairs a warp reads at once (256 B
+// apart in x) fall into different banks.
+__host__ __device__ constexpr int64_t xpad_floats(int64_t k) { return k + k / 64 * 4; }
+__device__ __forceinline__ int xpad_index(int e) { return e + (e >> 6) * 4; }
 
 struct B1Params {
   const uint8_t* W;
@@ -127,8 +133,8 @@ __device__ __forceinline__ unsigned long long qm8(uint32_t wa, uint32_t wb,
   return r;
 }
 
-// Dot product of block BLK (0 or 1) of a 36-byte block pair r[9] with the
-// activation pairs xp[16 * BLK ..]: returns sum_e (q_e - 8) * x_e as an fp32
+// Dot product of block BLK (0 or 1) of a 36-byte block pair r[9] (only the
+// words of that block are read) with its 16 activation pairs xb: returns sum_e (q_e - 8) * x_e as an fp32
 // pair (even and odd elements) and the block's scale in d.
 //   BLK 0: d = low half of r[0]; qs[0..1] high half of r[0], qs[2..13] in
 //          r[1..3], qs[14..15] low half of r[4].
@@ -136,9 +142,8 @@ __device__ __forceinline__ unsigned long long qm8(uint32_t wa, uint32_t wb,
 // Byte c of qs holds element c (low nibble) and element c + 16 (high nibble).
 template <int BLK>
 __device__ __forceinline__ unsigned long long block_dot(const uint32_t (&r)[9],
-                                                        const unsigned long long (&xp)[32],
+                                                        const unsigned long long (&xb)[16],
                                                         const DecodeConsts& c, float& d) {
-  const unsigned long long* xb = xp + 16 * BLK;
   unsigned long long acc;
   if constexpr (BLK == 0) {
     d = half_bits_to_float(r[0]);
@@ -175,9 +180,9 @@ __device__ __forceinline__ unsigned long long block_dot(const uint32_t (&r)[9],
   return acc;
 }
 
-__device__ __forceinline__ void ldg_nc_v2u64(const void* p, unsigned long long& a,
-                                             unsigned long long& b) {
-  asm volatile("ld.global.nc.v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p));
+__device__ __forceinline__ void lds_v2u64(uint32_t addr, unsigned long long& a,
+                                          unsigned long long& b) {
+  asm volatile("ld.shared.v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "r"(addr));
 }
 
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
@@ -195,36 +200,42 @@ __device__ __forceinline__ int64_t owner_of(int64_t u, int64_t units, int64_t wa
   return ((u + 1) * warps - 1) / units;
 }
 
-__global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
+__global__ void __launch_bounds__(kWarps * 32, 1)
     gemv_b1_kernel(const __grid_constant__ CUtensorMap tmap, const B1Params p) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t bars[kWarps][kStages];
   __shared__ __align__(8) uint64_t never[kWarps];  // test hook: nothing ever arrives here
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t wid = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
-  if (wid >= p.warps) {
-    pdl_allow_dependents();
-    return;
-  }
-  const uint32_t slots = smem_u32(smem) + warp * (kStages * kSlotBytes);
+  // Warps are dealt to CTAs round-robin so that small matrices still spread
+  // over every SM.
+  const int64_t wid = static_cast<int64_t>(warp) * gridDim.x + blockIdx.x;
+  const bool active = wid < p.warps;
+  const uint32_t xs = smem_u32(smem);
+  const int64_t xpad = xpad_floats(p.nsb * kSuperElems);
+  const uint32_t ring = xs + static_cast<uint32_t>((xpad * 4 + 127) / 128 * 128);
+  const uint32_t slots = ring + warp * (kStages * kSlotBytes);
   const uint32_t bar0 = smem_u32(&bars[warp][0]);
   const uint32_t never_bar = smem_u32(&never[warp]);
-  if (lane == 0) {
-    for (int s = 0; s < kStages; ++s) mbar_init(bar0 + 8 * s, 1);
-    mbar_init(never_bar, 1);
-    fence_mbarrier_init();
-  }
-  __syncwarp();
-
-  const int64_t u0 = range_start(wid, p.units, p.warps);
-  const int64_t nunits = range_start(wid + 1, p.units, p.warps) - u0;  // >= 1
   const uint64_t pol = l2_evict_first_policy();
   const bool stall_test = (p.flags & kFlagTestStallOneWait) != 0 && wid == 0;
-  const int64_t g_first = u0 / p.nsb;
 
-  // Producer side: the next unit to load, walked without divisions.
-  int64_t ig = g_first, isb = u0 - g_first * p.nsb, issued = 0;
+  int64_t u0 = 0, nunits = 0, g_first = 0;
+  int64_t ig = 0, isb = 0, issued = 0;
   int islot = 0;
+  if (active) {
+    if (lane == 0) {
+      for (int s = 0; s < kStages; ++s) mbar_init(bar0 + 8 * s, 1);
+      mbar_init(never_bar, 1);
+      fence_mbarrier_init();
+    }
+    __syncwarp();
+    u0 = range_start(wid, p.units, p.warps);
+    nunits = range_start(wid + 1, p.units, p.warps) - u0;  // >= 1
+    g_first = u0 / p.nsb;
+    ig = g_first;
+    isb = u0 - g_first * p.nsb;
+  }
+  // Producer side: the next unit to load, walked without divisions.
   auto issue_next = [&]() {
     if (lane == 0) {
       const uint32_t bar = bar0 + 8 * islot;
@@ -244,6 +255,21 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
   pdl_allow_dependents();
   pdl_wait_prior_grid();  // x, y and the workspace are now safe to touch
 
+  // Stage x (all of it) into shared memory with the padded layout.
+  {
+    const int64_t k4 = p.nsb * (kSuperElems / 4);
+    const float4* xg = reinterpret_cast<const float4*>(p.x);
+    for (int64_t i = threadIdx.x; i < k4; i += blockDim.x) {
+      const float4 v = __ldg(xg + i);
+      const int e = static_cast<int>(4 * i);
+      asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(xs + 4 * xpad_index(e)),
+                   "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
+                   : "memory");
+    }
+  }
+  __syncthreads();
+  if (!active) return;
+
   const DecodeConsts dc = make_consts();
   const int j = lane & 3;    // block pair within the unit
   const int rr = lane >> 2;  // rows rr, rr + 8, rr + 16, rr + 24 of the group
@@ -255,12 +281,6 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
   uint32_t parity = 0;
   bool ok = true;
   for (; done < nunits; ++done) {
-    unsigned long long xp[32];
-    {
-      const float* xs = p.x + sb * kSuperElems + 64 * j;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) ldg_nc_v2u64(xs + 4 * i, xp[2 * i], xp[2 * i + 1]);
-    }
     // every lane waits; the verdict is made warp-uniform before any __syncwarp.
     // The test hook waits on a barrier that nothing arrives on, so that wait
     // runs out after kWaitLimitNs.
@@ -271,21 +291,27 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
       break;
     }
     const uint32_t src = slots + slot * kSlotBytes + rr * kSuperBytes + 36 * j;
+    const int xe = static_cast<int>(sb * kSuperElems) + 64 * j;  // first element of the pair
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      uint32_t r[9];
+    for (int b = 0; b < 2; ++b) {
+      unsigned long long xb[16];
+      const uint32_t xa = xs + 4 * xpad_index(xe + 32 * b);
 #pragma unroll
-      for (int w = 0; w < 9; ++w) r[w] = lds32(src + i * 8 * kSuperBytes + 4 * w);
-      float d0, d1;
-      const f2 a0 = unpack2(block_dot<0>(r, xp, dc, d0));
-      const f2 a1 = unpack2(block_dot<1>(r, xp, dc, d1));
-      yv[i] = fmaf(a0.x + a0.y, d0, yv[i]);
-      yv[i] = fmaf(a1.x + a1.y, d1, yv[i]);
+      for (int i = 0; i < 8; ++i) lds_v2u64(xa + 16 * i, xb[2 * i], xb[2 * i + 1]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        uint32_t r[9];
+#pragma unroll
+        for (int w = 0; w < 5; ++w)
+          r[4 * b + w] = lds32(src + i * 8 * kSuperBytes + 4 * (4 * b + w));
+        float d;
+        const f2 a = unpack2(b == 0 ? block_dot<0>(r, xb, dc, d) : block_dot<1>(r, xb, dc, d));
+        yv[i] = fmaf(a.x + a.y, d, yv[i]);
+      }
     }
     __syncwarp();
     fence_proxy_async_smem();
     if (issued < nunits) issue_next();
-
     if (sb == p.nsb - 1 || done == nunits - 1) {
       // Row group g is done for this warp: the four lanes of a quad hold the
       // four block-pair sums of the same rows; add them (fixed order).
@@ -372,8 +398,13 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
 }  // namespace
 
 int64_t gemv_b1_warps(int64_t units) {
-  const int64_t target = static_cast<int64_t>(sm_count()) * kCtasPerSm * kWarps;
+  const int64_t target = static_cast<int64_t>(sm_count()) * kWarps;
   return units < target ? units : target;
+}
+
+bool gemv_b1_supports(int64_t k) {
+  const int64_t xbytes = (xpad_floats(k) * 4 + 127) / 128 * 128;
+  return xbytes + kRingBytes <= kMaxSmem;
 }
 
 cudaError_t gemv_b1_launch(const uint8_t* W, int64_t n, int64_t k, const float* x, float* y,
@@ -390,7 +421,7 @@ cudaError_t gemv_b1_launch(const uint8_t* W, int64_t n, int64_t k, const float* 
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
     cudaError_t e = cudaFuncSetAttribute(gemv_b1_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
@@ -407,9 +438,11 @@ cudaError_t gemv_b1_launch(const uint8_t* W, int64_t n, int64_t k, const float* 
   p.status = status;
   p.flags = flags;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>((warps + kWarps - 1) / kWarps));
+  const int64_t sms = sm_count();
+  cfg.gridDim = dim3(static_cast<unsigned>(warps < sms ? warps : sms));
   cfg.blockDim = dim3(kWarps * 32);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes =
+      static_cast<unsigned>((xpad_floats(k) * 4 + 127) / 128 * 128 + kRingBytes);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

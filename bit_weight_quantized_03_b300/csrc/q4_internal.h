@@ -41,6 +41,7 @@ cudaError_t gemv_launch(const GemvPlan& plan, const uint8_t* W, int64_t n, int64
                         void* workspace, int32_t* status, uint32_t flags, cudaStream_t s);
 
 int64_t gemv_b1_warps(int64_t units);
+bool gemv_b1_supports(int64_t k);
 cudaError_t gemv_b1_launch(const uint8_t* W, int64_t n, int64_t k, const float* x, float* y,
                            int32_t* counters, float* partials, int64_t units, int64_t warps,
                            int32_t* status, uint32_t flags, cudaStream_t s);
