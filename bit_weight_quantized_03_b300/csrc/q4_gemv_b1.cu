@@ -185,6 +185,13 @@ __device__ __forceinline__ void lds_v2u64(uint32_t addr, unsigned long long& a,
   asm volatile("ld.shared.v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "r"(addr));
 }
 
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int32_t* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
+               : "memory");
+  return old;
+}
+
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
   uint32_t v;
   asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
@@ -339,15 +346,14 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
 #pragma unroll
           for (int i = 0; i < 4; ++i) __stcg(mine + rr + 8 * i, v[i]);
         }
-        __threadfence();
-        __syncwarp();
+        __syncwarp();  // the lanes' partials are ordered before lane 0's release
         const int64_t i0 = owner_of(gu0, p.units, p.warps);
         const int64_t i1 = owner_of(gu1 - 1, p.units, p.warps);
         int last = 0;
-        if (lane == 0) last = atomicAdd(&p.counters[g], 1) == static_cast<int>(i1 - i0);
+        // acq_rel: releases this warp's partials; the last arrival acquires all
+        if (lane == 0) last = atomic_add_acq_rel_gpu(&p.counters[g], 1) == static_cast<int>(i1 - i0);
         last = __shfl_sync(0xffffffffu, last, 0);
         if (last) {
-          __threadfence();
           // Owner i0 may have started in an earlier group (then this group is
           // its slot 1); every later owner starts inside this group (slot 0).
           const int64_t i0_slot = range_start(i0, p.units, p.warps) < gu0 ? 1 : 0;
