@@ -257,22 +257,35 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     }
     if (++islot == kStages) islot = 0;
   };
-  while (issued < nunits && issued < kStages) issue_next();
-
   pdl_allow_dependents();
   pdl_wait_prior_grid();  // x, y and the workspace are now safe to touch
 
-  // Stage x (all of it) into shared memory with the padded layout.
+  // Stage x (all of it) into shared memory with the padded layout.  Its loads
+  // are issued before the weight stream starts, so that they are not queued
+  // behind the first units' tile loads.
   {
-    const int64_t k4 = p.nsb * (kSuperElems / 4);
+    constexpr int kXRegs = 5;  // covers k <= 5 * 4 * 512 = 10240 in one pass
+    const int k4 = static_cast<int>(p.nsb * (kSuperElems / 4));
     const float4* xg = reinterpret_cast<const float4*>(p.x);
-    for (int64_t i = threadIdx.x; i < k4; i += blockDim.x) {
-      const float4 v = __ldg(xg + i);
-      const int e = static_cast<int>(4 * i);
-      asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(xs + 4 * xpad_index(e)),
+    float4 xv[kXRegs];
+#pragma unroll
+    for (int t = 0; t < kXRegs; ++t) {
+      const int i = static_cast<int>(threadIdx.x) + t * kWarps * 32;
+      if (i < k4) xv[t] = __ldg(xg + i);
+    }
+    while (issued < nunits && issued < kStages) issue_next();
+    auto put = [&](int i, const float4& v) {
+      asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(xs + 4 * xpad_index(4 * i)),
                    "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
                    : "memory");
+    };
+#pragma unroll
+    for (int t = 0; t < kXRegs; ++t) {
+      const int i = static_cast<int>(threadIdx.x) + t * kWarps * 32;
+      if (i < k4) put(i, xv[t]);
     }
+    for (int i = static_cast<int>(threadIdx.x) + kXRegs * kWarps * 32; i < k4; i += kWarps * 32)
+      put(i, __ldg(xg + i));
   }
   __syncthreads();
   if (!active) return;
