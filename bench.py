@@ -252,6 +252,8 @@ def run_ours(args):
     gemm = None
     if args.only in ("all", "gemm"):
         gemm = _run_gemm(args, world, dev, stream, bf16_burst, bf16_sust, peak_src, torch)
+    if args.only in ("all", "crossover"):
+        line["crossover"] = _run_crossover(args, dev, stream, hbm, bf16_burst, torch)
     cpu = None
     if rank == 0 and world == 1 and args.cpu_seconds > 0:
         cpu = _oracle_sample(seconds=args.cpu_seconds)
@@ -397,34 +399,91 @@ def _run_head_gather(args, dev, stream, hbm, torch):
 
 
 def _run_gemm(args, world, dev, stream, bf16_burst, bf16_sust, peak_src, torch):
+    """Encoder/prefill GEMM stack at M = 375, 1500 and 3000 frames (headline: 3000)."""
     import synth
     from bit_weight_quantized_03_b300.stacks import EncoderStack
 
-    # ---------------- prefill / encoder GEMM
-    gemm = None
-    if True:
-        M = 3000
-        try:
-            enc = EncoderStack(frames=M, device=dev)
+    try:
+        enc = EncoderStack(frames=3000, device=dev)
+        per_m = {}
+        for M in (375, 1500, 3000):
             x0 = synth.torch_activations(M, 1280, seed=synth.activation_seed(4000), device=dev,
                                          dtype=torch.bfloat16)
             ge = enc.capture(x0, stream)
             _time_graph_replays([(ge, 2)], stream, torch)
             _barrier(world)
             gms = _barrier_max(_time_graph_replays([(ge, 5)], stream, torch) / 5, world, torch)
-            tflops = enc.flops_per_pass() / (gms * 1e-3) / 1e12
-            gemm = {"workload": f"encoder linear stack, 32 layers x (qkv 1280->3840, out "
-                                f"1280->1280, up 1280->5120, down 5120->1280), M={M} frames",
-                    "value": world * tflops, "unit": "TFLOP/s", "ms_per_pass": gms,
-                    "roofline": {"bound": "tensor", "achieved": tflops, "peak": bf16_burst,
-                                 "unit": "TFLOP/s", "frac": tflops / bf16_burst,
-                                 "peak_source": f"{peak_src} bf16 burst"},
-                    "frac_of_sustained": tflops / bf16_sust,
-                    "gpu_launches_per_pass": enc.launches_per_pass()}
-            del enc, ge
-        except Exception as e:  # reported, never silently replaced
-            gemm = {"error": f"{type(e).__name__}: {e}"}
+            per_m[M] = (gms, enc.flops(M) / (gms * 1e-3) / 1e12)
+            del ge
+        gms, tflops = per_m[3000]
+        gemm = {"workload": "encoder linear stack, 32 layers x (qkv 1280->3840, out "
+                            "1280->1280, up 1280->5120, down 5120->1280), M=3000 frames",
+                "value": world * tflops, "unit": "TFLOP/s", "ms_per_pass": gms,
+                "roofline": {"bound": "tensor", "achieved": tflops, "peak": bf16_burst,
+                             "unit": "TFLOP/s", "frac": tflops / bf16_burst,
+                             "kernel": "gemm_tc_kernel",
+                             "peak_source": f"{peak_src} bf16 burst (cuBLAS 8192^3)"},
+                "frac_of_sustained": tflops / bf16_sust,
+                "by_frames": {str(M): {"ms_per_pass": v[0], "tflops": v[1],
+                                       "frac_of_peak": v[1] / bf16_burst}
+                              for M, v in per_m.items()},
+                "gpu_launches_per_pass": enc.launches_per_pass()}
+        del enc
+    except Exception as e:  # reported, never silently replaced
+        gemm = {"error": f"{type(e).__name__}: {e}"}
     return gemm
+
+
+def _run_crossover(args, dev, stream, hbm, bf16_burst, torch):
+    """Batched decode on the 4096x3072 decoder shape: fp32 GEMV vs bf16 tensor-core
+    GEMM for M in 1..128 concurrent streams, L2-cold (72 weight copies, 510 MB)."""
+    import synth
+    from bit_weight_quantized_03_b300 import (FLAG_PDL, GEMV_MAX_M, Workspace, q4_gemm, q4_gemv,
+                                              q4_quantize)
+    n, k, copies, reps = 4096, 3072, 72, 72
+    Ws = []
+    for c in range(copies):
+        w = synth.torch_weights(n, k, seed=synth.seed_for(5, 0, c), device=dev)
+        Ws.append(q4_quantize(w))
+        del w
+    wbytes = n * k // 32 * 18
+    ws = Workspace(dev)
+    rows = {}
+    for M in (1, 2, 4, 8, 16, 32, 64, 128):
+        x32 = synth.torch_activations(M, k, seed=synth.activation_seed(5000, M), device=dev)
+        xbf = x32.to(torch.bfloat16)
+        y = torch.empty((M, n), device=dev)
+        res = {}
+        paths = [("gemm", lambda W: q4_gemm(W, n, k, xbf, Y=y, workspace=ws, flags=FLAG_PDL,
+                                           stream=stream))]
+        if M <= GEMV_MAX_M:
+            paths.insert(0, ("gemv", lambda W: q4_gemv(W, n, k, x32, y=y, workspace=ws,
+                                                       flags=FLAG_PDL, stream=stream)))
+        for name, fn in paths:
+            with torch.cuda.stream(stream):
+                fn(Ws[0])
+                stream.synchronize()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    for i in range(reps):
+                        fn(Ws[i % copies])
+            _time_graph_replays([(g, 1)], stream, torch)
+            us = _time_graph_replays([(g, 3)], stream, torch) / (3 * reps) * 1e3
+            byts = wbytes + M * k * (4 if name == "gemv" else 2) + M * n * 4
+            res[name] = {"us": us, "gbs": byts / (us * 1e-6) / 1e9,
+                         "tflops": 2 * M * n * k / (us * 1e-6) / 1e12}
+            del g
+        rows[str(M)] = res
+    cross = None
+    for M in (1, 2, 4, 8, 16, 32, 64, 128):
+        r = rows[str(M)]
+        if "gemv" not in r or r["gemm"]["us"] < r["gemv"]["us"]:
+            cross = M
+            break
+    return {"workload": "batched decode, 4096x3072 Q4_0, M concurrent streams, fp32 x (GEMV) / "
+                        "bf16 x (tensor-core GEMM), fp32 y; 72 weight copies rotated (L2-cold)",
+            "by_m": rows, "crossover_m": cross,
+            "note": "crossover_m = smallest M at which the tensor-core GEMM is faster"}
 
 
 def main():
@@ -433,7 +492,8 @@ def main():
     ap.add_argument("--steps", type=int, default=256)
     ap.add_argument("--warmup", type=int, default=16)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--only", choices=["all", "stack", "head", "gather", "gemm"], default="all",
+    ap.add_argument("--only", choices=["all", "stack", "head", "gather", "gemm", "crossover"],
+                    default="all",
                     help="run one section (profiling runs); the default runs all of them")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--traffic", type=float, default=None,

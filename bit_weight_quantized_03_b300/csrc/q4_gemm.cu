@@ -6,47 +6,51 @@
 // "Arquitectura"), so with hundreds to thousands of frames the product is a
 // dense contraction and belongs on the tcgen05 tensor cores.
 //
-// One CTA computes a 128 (weight rows) x BN (tokens) tile over the whole k:
-//   warp 0   TMA producer: packed Q4 rows (2-D map over the bytes, box 144 B x
-//            128 rows = 256 weights per row) and bf16 X tiles (box 64 x BN,
-//            128-byte swizzle), each into a ring guarded by mbarriers.
-//   warp 1   owns the tensor memory and issues tcgen05.mma (kind::f16, bf16 in,
-//            fp32 accumulate in TMEM) from one thread; tcgen05.commit releases
-//            the ring slots.
-//   warps 2-5  dequantize: thread t decodes row t of the packed tile to exact
-//            fp32 (q - 8) * d, rounds to bf16 and writes the K-major 128-byte-
-//            swizzled operand layout the MMA descriptor expects; then they run
-//            the epilogue (tcgen05.ld 32x32b, fp32 or bf16 stores).
-// The weight tile is the MMA's M side (128 rows) and the tokens its N side, so
-// one dequantization serves BN tokens.  Every wait is bounded; on expiry the
-// CTA reports Q4_ERR_TIMEOUT, drains its copies and MMAs, frees TMEM and exits.
+// Persistent kernel, one CTA per SM, each CTA looping over output tiles of
+// 128 weight rows (MMA M) x BN tokens (MMA N, a multiple of 32 up to 224,
+// picked per shape so that the tiles fill the SMs in whole waves):
+//   warp 0     TMA producer: packed Q4 rows (2-D map over the bytes, box
+//              144 B x 128 rows = 256 weights per row) and bf16 X tiles (box
+//              64 x BN, 128-byte swizzle), each into a ring of mbarrier-guarded
+//              shared-memory stages.
+//   warp 1     allocates all 512 TMEM columns and issues tcgen05.mma
+//              (kind::f16: A = the dequantized weights, read from TMEM; B = the
+//              X tile, read from shared memory; fp32 accumulator in TMEM) from
+//              one thread; tcgen05.commit releases the stages.
+//   warps 2-9  dequantize: thread t of a warp in TMEM lane quarter q decodes row
+//              32q + t to exact fp32 (q - 8) * d, rounds to bf16 and writes the
+//              64 weights of a k-step to its TMEM lane with one tcgen05.st.
+//              Warps 2-5 produce the even k-steps, warps 6-9 the odd ones, into
+//              two TMEM A stages.
+//   warps 10-13  epilogue: tcgen05.ld of the finished accumulator, fp32 or bf16
+//              stores (consecutive rows per warp store).
+// Keeping A in TMEM leaves shared memory to the X operand only, whose traffic
+// (64 tokens-bytes in, the same out per 64 k) is what bounds a 128-row MMA.
+// Two accumulators (columns [0, 224) and [224, 448)) let the epilogue of one
+// tile overlap the main loop of the next; the A stages sit at columns 448 and
+// 480.  Every wait is bounded; on expiry the CTA reports Q4_ERR_TIMEOUT, lets
+// its copies and MMAs drain, frees TMEM and exits.
+#include <type_traits>
+
 #include "q4_device.cuh"
 
 namespace q4 {
 namespace {
 
-constexpr int kThreads = 192;
-constexpr int kTileRows = 128;       // weight rows per tile (MMA M)
-constexpr int kKStep = 64;           // weights per MMA stage (128 B of bf16 per row)
-constexpr int kStagesX = 4;
-constexpr int kStagesA = 3;
+constexpr int kThreads = 14 * 32;
+constexpr int kTileRows = 128;  // weight rows per tile (MMA M)
+constexpr int kKStep = 64;      // weights per k-step (128 B of bf16 per row)
 constexpr int kStagesW = 2;
 constexpr int kPackedStageBytes = kTileRows * kSuperBytes;  // 18432
-constexpr int kATileBytes = kTileRows * 128;                // 16384
-
-template <int BN>
-struct Smem {
-  static constexpr int kXTileBytes = BN * 128;
-  static constexpr int kX = 0;
-  static constexpr int kA = kX + kStagesX * kXTileBytes;
-  static constexpr int kW = kA + kStagesA * kATileBytes;
-  static constexpr int kBars = kW + kStagesW * kPackedStageBytes;
-  // barriers: x_full, x_empty, a_full, a_empty, w_full, w_empty, d_full, drain
-  static constexpr int kNumBars = 2 * kStagesX + 2 * kStagesA + 2 * kStagesW + 2;
-  static constexpr int kMisc = kBars + 8 * kNumBars;
-  static constexpr int kBytes = kMisc + 16;
-  static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1024
-};
+constexpr int kMaxBN = 224;
+constexpr uint32_t kTmemCols = 512;
+// TMEM columns: accumulator b at acc_col(b), A stage p at a_col(p).
+__host__ __device__ constexpr uint32_t acc_col(int b) { return static_cast<uint32_t>(b) * 224u; }
+__host__ __device__ constexpr uint32_t a_col(int p) { return 448u + 32u * static_cast<uint32_t>(p); }
+constexpr int kAStages = 2;  // one 64-weight k-step (32 columns) each
+constexpr int kMaxXStages = 8;
+constexpr int kSmemBudget = 226 * 1024;
+constexpr int kBarBytes = 1024;  // barriers and flags, after the rings
 
 // ------------------------------------------------------------ PTX wrappers
 
@@ -68,13 +72,14 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                          uint32_t idesc, uint32_t accumulate) {
+// D (TMEM) [+]= A (TMEM) x B (shared-memory descriptor)
+__device__ __forceinline__ void umma_ts_bf16(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                             uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
@@ -82,13 +87,31 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
       : "memory");
 }
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-      "%11, %12, %13, %14, %15}, [%16];"
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, "
+      "%29, %30, %31, %32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),
+      "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),
+      "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, "
+      "%29, %30, %31}, [%32];"
       : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
         "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
-        "=r"(v[14]), "=r"(v[15])
+        "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),
+        "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
+        "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
       : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_ld_wait() {
@@ -104,12 +127,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
 }
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
-}
-__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                       uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-               "r"(d)
-               : "memory");
 }
 __device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
   uint32_t r;
@@ -140,72 +157,59 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int m, int n) {
 
 // ------------------------------------------------------------ dequant helpers
 
+// Weights (q-8)*d of a pair, exact in fp32, rounded to bf16 and packed.
 template <int PA, int PB>
-__device__ __forceinline__ uint32_t wq_bf16x2(uint32_t wa, uint32_t wb, float d) {
-  // exact (q - 8) for the two nibbles, times d (exact in fp32), rounded to bf16
-  const unsigned long long qm8 =
-      fsub2(pack2(nibble_magic<PA>(wa), nibble_magic<PB>(wb)),
-            pack2(NibbleMagic<PA>::kBias, NibbleMagic<PB>::kBias));
-  const f2 w = unpack2(fmul2(qm8, pack2(d, d)));
+__device__ __forceinline__ uint32_t wq_bf16x2(uint32_t wa, uint32_t wb, const DecodeConsts& c,
+                                              unsigned long long d2) {
+  const f2 w = unpack2(fmul2(qm8<PA, PB>(wa, wb, c), d2));
   return bf16x2_rn(w.x, w.y);
 }
 
 // Decodes block BLK (0..7) of a 144-byte run r[36] into 16 bf16x2 words:
-// out[e/2] = (w[e], w[e+1]) for e even.
+// o[e/2] = (w[e], w[e+1]) for e even.  Byte c of qs holds element c (low
+// nibble) and element c + 16 (high nibble).
 template <int BLK>
-__device__ __forceinline__ void decode_block_bf16(const uint32_t (&r)[36], uint32_t (&o)[16]) {
-  constexpr int ob = 18 * BLK;
+__device__ __forceinline__ void decode_block_bf16(const uint32_t (&r)[36], const DecodeConsts& c,
+                                                  uint32_t* o) {
+  constexpr int ob = 18 * BLK;  // byte offset of the block in the run
   constexpr int wd = ob / 4;
   constexpr bool d_high = ((ob / 2) & 1) != 0;
   const float d = half_bits_to_float(d_high ? (r[wd] >> 16) : r[wd]);
+  const unsigned long long d2 = pack2(d, d);
   if constexpr ((BLK & 1) == 1) {
+    // qs starts 4-byte aligned: word i holds qs[4i .. 4i+3]
     constexpr int w0 = (ob + 2) / 4;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const uint32_t w = r[w0 + i], t = w >> 12;
-      o[2 * i] = wq_bf16x2<0, 8>(w, w, d);
-      o[2 * i + 1] = wq_bf16x2<16, 12>(w, t, d);
-      o[8 + 2 * i] = wq_bf16x2<4, 12>(w, w, d);
-      o[8 + 2 * i + 1] = wq_bf16x2<8, 16>(t, t, d);
+      const uint32_t w = r[w0 + i], t = shr12(w);
+      o[2 * i] = wq_bf16x2<0, 8>(w, w, c, d2);           // elements 4i, 4i+1
+      o[2 * i + 1] = wq_bf16x2<16, 12>(w, t, c, d2);     // 4i+2, 4i+3
+      o[8 + 2 * i] = wq_bf16x2<4, 12>(w, w, c, d2);      // 4i+16, 4i+17
+      o[8 + 2 * i + 1] = wq_bf16x2<8, 16>(t, t, c, d2);  // 4i+18, 4i+19
     }
   } else {
+    // qs starts 2 bytes into a word: qs[0..1] in the high half of word ob/4,
+    // qs[2..13] in the next three words, qs[14..15] in the low half after them
     constexpr int w0 = ob / 4;
     {
-      const uint32_t w = r[w0], t = w >> 12;
-      o[0] = wq_bf16x2<16, 12>(w, t, d);
-      o[8] = wq_bf16x2<8, 16>(t, t, d);
+      const uint32_t w = r[w0], t = shr12(w);
+      o[0] = wq_bf16x2<16, 12>(w, t, c, d2);  // elements 0, 1
+      o[8] = wq_bf16x2<8, 16>(t, t, c, d2);   // 16, 17
     }
 #pragma unroll
     for (int i = 0; i < 3; ++i) {
-      const uint32_t w = r[w0 + 1 + i], t = w >> 12;
-      o[1 + 2 * i] = wq_bf16x2<0, 8>(w, w, d);
-      o[2 + 2 * i] = wq_bf16x2<16, 12>(w, t, d);
-      o[9 + 2 * i] = wq_bf16x2<4, 12>(w, w, d);
-      o[10 + 2 * i] = wq_bf16x2<8, 16>(t, t, d);
+      const uint32_t w = r[w0 + 1 + i], t = shr12(w);  // qs[2+4i .. 5+4i]
+      o[1 + 2 * i] = wq_bf16x2<0, 8>(w, w, c, d2);     // 2+4i, 3+4i
+      o[2 + 2 * i] = wq_bf16x2<16, 12>(w, t, c, d2);   // 4+4i, 5+4i
+      o[9 + 2 * i] = wq_bf16x2<4, 12>(w, w, c, d2);    // 18+4i, 19+4i
+      o[10 + 2 * i] = wq_bf16x2<8, 16>(t, t, c, d2);   // 20+4i, 21+4i
     }
     {
       const uint32_t w = r[w0 + 4];
-      o[7] = wq_bf16x2<0, 8>(w, w, d);
-      o[15] = wq_bf16x2<4, 12>(w, w, d);
+      o[7] = wq_bf16x2<0, 8>(w, w, c, d2);   // 14, 15
+      o[15] = wq_bf16x2<4, 12>(w, w, c, d2); // 30, 31
     }
   }
-}
-
-// Writes the 64 weights (blocks B0, B0+1 of the run) of row `row` into an A
-// tile: 8 chunks of 16 B, chunk c at row*128 + ((c ^ (row & 7)) * 16).
-template <int B0>
-__device__ __forceinline__ void write_a_kstep(const uint32_t (&r)[36], uint32_t a_tile, int row) {
-  uint32_t o0[16], o1[16];
-  decode_block_bf16<B0>(r, o0);
-  decode_block_bf16<B0 + 1>(r, o1);
-  const uint32_t base = a_tile + row * 128;
-  const int sw = row & 7;
-#pragma unroll
-  for (int c = 0; c < 4; ++c)
-    sts128(base + ((c ^ sw) << 4), o0[4 * c], o0[4 * c + 1], o0[4 * c + 2], o0[4 * c + 3]);
-#pragma unroll
-  for (int c = 0; c < 4; ++c)
-    sts128(base + (((c + 4) ^ sw) << 4), o1[4 * c], o1[4 * c + 1], o1[4 * c + 2], o1[4 * c + 3]);
 }
 
 struct GemmArgs {
@@ -213,60 +217,78 @@ struct GemmArgs {
   void* y;
   int32_t* status;
   int y_bf16;
+  int bn;         // tokens per tile (multiple of 32, <= kMaxBN)
+  int n_tiles;    // tiles along the weight rows
+  int tiles;      // n_tiles x token tiles
+  int x_stages;   // X ring depth
 };
 
-template <int BN>
+struct Bars {
+  uint32_t w_full, w_empty, x_full, x_empty, a_full, a_empty, acc_full, acc_empty, drain;
+};
+
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
                    const __grid_constant__ CUtensorMap tmap_x, const GemmArgs args) {
-  using L = Smem<BN>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
-  const uint32_t xs = base + L::kX, as = base + L::kA, wsm = base + L::kW;
-  const uint32_t bars = base + L::kBars;
-  const uint32_t x_full = bars, x_empty = x_full + 8 * kStagesX;
-  const uint32_t a_full = x_empty + 8 * kStagesX, a_empty = a_full + 8 * kStagesA;
-  const uint32_t w_full = a_empty + 8 * kStagesA, w_empty = w_full + 8 * kStagesW;
-  const uint32_t d_full = w_empty + 8 * kStagesW, drain = d_full + 8;
-  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gbase + L::kMisc);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + L::kMisc + 4);
+  const int nx = args.x_stages;
+  const uint32_t x_tile_bytes = static_cast<uint32_t>(args.bn) * 128u;
+  const uint32_t xs = base;                                    // X ring
+  const uint32_t wsm = xs + static_cast<uint32_t>(nx) * x_tile_bytes;  // packed W ring
+  const uint32_t bar_base = wsm + kStagesW * kPackedStageBytes;
+  Bars B;
+  B.w_full = bar_base;
+  B.w_empty = B.w_full + 8 * kStagesW;
+  B.x_full = B.w_empty + 8 * kStagesW;
+  B.x_empty = B.x_full + 8 * kMaxXStages;
+  B.a_full = B.x_empty + 8 * kMaxXStages;
+  B.a_empty = B.a_full + 8 * kAStages;
+  B.acc_full = B.a_empty + 8 * kAStages;
+  B.acc_empty = B.acc_full + 16;
+  B.drain = B.acc_empty + 16;
+  const uint32_t misc = B.drain + 8;
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gbase + (misc - base));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + (misc - base) + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t n0 = static_cast<int64_t>(blockIdx.x) * kTileRows;
-  const int64_t m0 = static_cast<int64_t>(blockIdx.y) * BN;
   const int ksteps = static_cast<int>(args.k / kKStep);
-  constexpr uint32_t kTmemCols = BN <= 32 ? 32 : (BN <= 64 ? 64 : (BN <= 128 ? 128 : 256));
+  const int wstages = ksteps / 4;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStagesX; ++s) {
-      mbar_init(x_full + 8 * s, 1);
-      mbar_init(x_empty + 8 * s, 1);
-    }
-    for (int s = 0; s < kStagesA; ++s) {
-      mbar_init(a_full + 8 * s, 4);
-      mbar_init(a_empty + 8 * s, 1);
-    }
     for (int s = 0; s < kStagesW; ++s) {
-      mbar_init(w_full + 8 * s, 1);
-      mbar_init(w_empty + 8 * s, 4);
+      mbar_init(B.w_full + 8 * s, 1);
+      mbar_init(B.w_empty + 8 * s, 8);
     }
-    mbar_init(d_full, 1);
-    mbar_init(drain, 1);
+    for (int s = 0; s < nx; ++s) {
+      mbar_init(B.x_full + 8 * s, 1);
+      mbar_init(B.x_empty + 8 * s, 1);
+    }
+    for (int s = 0; s < kAStages; ++s) {
+      mbar_init(B.a_full + 8 * s, 4);
+      mbar_init(B.a_empty + 8 * s, 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(B.acc_full + 8 * s, 1);
+      mbar_init(B.acc_empty + 8 * s, 4);
+    }
+    mbar_init(B.drain, 1);
     *abort_flag = 0;
     fence_mbarrier_init();
     prefetch_tmap(&tmap_w);
     prefetch_tmap(&tmap_x);
   }
   if (warp == 1) {
-    tmem_alloc(base + L::kMisc, kTmemCols);
+    tmem_alloc(misc, kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const int cta = static_cast<int>(blockIdx.x), ncta = static_cast<int>(gridDim.x);
 
   pdl_allow_dependents();
   pdl_wait_prior_grid();
@@ -275,140 +297,189 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (atomicExch(const_cast<int*>(abort_flag), 1) == 0) report(args.status, 6);
   };
 
-  if (warp == 0 && lane == 0) {
-    // ---------------- producer
-    int issued_x = 0, issued_w = 0;
-    bool ok = true;
-    for (int ks = 0; ks < ksteps && ok; ++ks) {
-      if ((ks & 3) == 0) {
-        const int j = ks >> 2, s = j % kStagesW;
-        if (!mbar_wait(w_empty + 8 * s, ((j / kStagesW) & 1) ^ 1, abort_flag)) {
-          ok = false;
-          break;
-        }
-        mbar_arrive_expect_tx(w_full + 8 * s, kPackedStageBytes);
-        tma_load_2d(wsm + s * kPackedStageBytes, &tmap_w, j * kSuperBytes,
-                    static_cast<int32_t>(n0), w_full + 8 * s);
-        ++issued_w;
-      }
-      const int s = ks % kStagesX;
-      if (!mbar_wait(x_empty + 8 * s, ((ks / kStagesX) & 1) ^ 1, abort_flag)) {
-        ok = false;
-        break;
-      }
-      mbar_arrive_expect_tx(x_full + 8 * s, L::kXTileBytes);
-      tma_load_2d(xs + s * L::kXTileBytes, &tmap_x, ks * kKStep, static_cast<int32_t>(m0),
-                  x_full + 8 * s);
-      ++issued_x;
-    }
-    if (!ok) {
-      fail();
-      // let issued copies land before the CTA can exit
-      for (int i = issued_x - kStagesX > 0 ? issued_x - kStagesX : 0; i < issued_x; ++i)
-        mbar_wait(x_full + 8 * (i % kStagesX), (i / kStagesX) & 1);
-      for (int i = issued_w - kStagesW > 0 ? issued_w - kStagesW : 0; i < issued_w; ++i)
-        mbar_wait(w_full + 8 * (i % kStagesW), (i / kStagesW) & 1);
-    }
-  } else if (warp == 1 && lane == 0) {
-    // ---------------- MMA issuer
-    constexpr uint32_t idesc = idesc_bf16(kTileRows, BN);
-    bool ok = true, any = false;
-    for (int ks = 0; ks < ksteps; ++ks) {
-      const int sa = ks % kStagesA, sx = ks % kStagesX;
-      if (!mbar_wait(a_full + 8 * sa, (ks / kStagesA) & 1, abort_flag) ||
-          !mbar_wait(x_full + 8 * sx, (ks / kStagesX) & 1, abort_flag)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const uint64_t adesc = sw128_desc(as + sa * kATileBytes);
-      const uint64_t bdesc = sw128_desc(xs + sx * L::kXTileBytes);
-#pragma unroll
-      for (int kk = 0; kk < kKStep / 16; ++kk)
-        umma_bf16(tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (ks | kk) != 0);
-      any = true;
-      umma_commit(x_empty + 8 * sx);
-      umma_commit(a_empty + 8 * sa);
-    }
-    if (ok) {
-      umma_commit(d_full);
-    } else {
-      fail();
-    }
-    if (any) {  // every MMA has finished reading shared memory before exit
-      umma_commit(drain);
-      mbar_wait(drain, 0);
-    }
-  } else if (warp >= 2) {
-    // ---------------- dequantize, then epilogue
-    const int row = threadIdx.x - 64;  // 0..127
-    bool ok = true;
-    for (int j = 0; j < ksteps / 4 && ok; ++j) {
-      const int s = j % kStagesW;
-      const bool landed = mbar_wait(w_full + 8 * s, (j / kStagesW) & 1, abort_flag);
-      if (!__all_sync(0xffffffffu, landed)) {  // warp-uniform verdict
-        ok = false;
-        break;
-      }
-      uint32_t r[36];
-      const uint32_t src = wsm + s * kPackedStageBytes + row * kSuperBytes;
-#pragma unroll
-      for (int i = 0; i < 9; ++i) {
-        const uint4 v = lds128(src + 16 * i);
-        r[4 * i + 0] = v.x;
-        r[4 * i + 1] = v.y;
-        r[4 * i + 2] = v.z;
-        r[4 * i + 3] = v.w;
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(w_empty + 8 * s);
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const int ks = 4 * j + kk, sa = ks % kStagesA;
-        const bool free_slot = mbar_wait(a_empty + 8 * sa, ((ks / kStagesA) & 1) ^ 1, abort_flag);
-        if (!__all_sync(0xffffffffu, free_slot)) {
-          ok = false;
-          break;
-        }
-        const uint32_t a_tile = as + sa * kATileBytes;
-        if (kk == 0) write_a_kstep<0>(r, a_tile, row);
-        if (kk == 1) write_a_kstep<2>(r, a_tile, row);
-        if (kk == 2) write_a_kstep<4>(r, a_tile, row);
-        if (kk == 3) write_a_kstep<6>(r, a_tile, row);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(a_full + 8 * sa);
-      }
-    }
-    if (!ok) fail();
-    const bool done = ok && mbar_wait(d_full, 0, abort_flag);
-    if (__all_sync(0xffffffffu, done)) {
-      tc_fence_after();
-      const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
-      const int64_t grow = n0 + 32 * quarter + lane;
-      const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * quarter) << 16);
-#pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 16) {
-        uint32_t v[16];
-        tmem_ld16(tbase + c0, v);
-        tmem_ld_wait();
-        if (grow < args.n) {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int64_t t = m0 + c0 + j;
-            if (t < args.m) {
-              if (args.y_bf16)
-                static_cast<__nv_bfloat16*>(args.y)[t * args.ldy + grow] =
-                    __float2bfloat16_rn(__uint_as_float(v[j]));
-              else
-                static_cast<float*>(args.y)[t * args.ldy + grow] = __uint_as_float(v[j]);
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer
+      int wj = 0, xk = 0;
+      bool ok = true;
+      for (int t = cta; t < args.tiles && ok; t += ncta) {
+        const int32_t n0 = (t % args.n_tiles) * kTileRows;
+        const int32_t m0 = (t / args.n_tiles) * args.bn;
+        for (int j = 0; j < wstages && ok; ++j) {
+          const int s = wj % kStagesW;
+          if (!mbar_wait(B.w_empty + 8 * s, ((wj / kStagesW) & 1) ^ 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(B.w_full + 8 * s, kPackedStageBytes);
+          tma_load_2d(wsm + s * kPackedStageBytes, &tmap_w, j * kSuperBytes, n0, B.w_full + 8 * s);
+          ++wj;
+          for (int kk = 0; kk < 4; ++kk) {
+            const int s2 = xk % nx;
+            if (!mbar_wait(B.x_empty + 8 * s2, ((xk / nx) & 1) ^ 1, abort_flag)) {
+              ok = false;
+              break;
             }
+            mbar_arrive_expect_tx(B.x_full + 8 * s2, x_tile_bytes);
+            tma_load_2d(xs + s2 * x_tile_bytes, &tmap_x, (4 * j + kk) * kKStep, m0,
+                        B.x_full + 8 * s2);
+            ++xk;
           }
         }
       }
-    } else if (ok) {
-      fail();
+      if (!ok) {
+        fail();
+        // let the copies still in flight land before the CTA can exit
+        for (int i = wj - kStagesW > 0 ? wj - kStagesW : 0; i < wj; ++i)
+          mbar_wait(B.w_full + 8 * (i % kStagesW), (i / kStagesW) & 1);
+        for (int i = xk - nx > 0 ? xk - nx : 0; i < xk; ++i)
+          mbar_wait(B.x_full + 8 * (i % nx), (i / nx) & 1);
+      }
     }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer
+      const uint32_t idesc = idesc_bf16(kTileRows, args.bn);
+      int xk = 0, iter = 0;
+      int a_use0 = 0, a_use1 = 0;  // completed uses of A stage 0 / 1
+      bool ok = true, any = false;
+      for (int t = cta; t < args.tiles && ok; t += ncta, ++iter) {
+        const int b = iter & 1;
+        if (!mbar_wait(B.acc_empty + 8 * b, ((iter >> 1) & 1) ^ 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int ks = 0; ks < ksteps; ++ks) {
+          const int p = ks & 1, s2 = xk % nx;
+          const int use = p ? a_use1 : a_use0;
+          if (!mbar_wait(B.a_full + 8 * p, use & 1, abort_flag) ||
+              !mbar_wait(B.x_full + 8 * s2, (xk / nx) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t bdesc = sw128_desc(xs + s2 * x_tile_bytes);
+#pragma unroll
+          for (int kk = 0; kk < kKStep / 16; ++kk)
+            umma_ts_bf16(tmem + acc_col(b), tmem + a_col(p) + 8 * kk, bdesc + 2 * kk, idesc,
+                         (ks | kk) != 0);
+          any = true;
+          umma_commit(B.x_empty + 8 * s2);
+          umma_commit(B.a_empty + 8 * p);
+          if (p) ++a_use1; else ++a_use0;
+          ++xk;
+        }
+        if (ok) umma_commit(B.acc_full + 8 * b);
+      }
+      if (!ok) fail();
+      if (any) {  // every MMA has finished with TMEM and shared memory before exit
+        umma_commit(B.drain);
+        mbar_wait(B.drain, 0);
+      }
+    }
+  } else if (warp < 10) {
+    // ---------------- dequantize into the TMEM A stages
+    const int q = warp & 3;         // TMEM lane quarter
+    const int p = (warp - 2) >> 2;  // 0: even k-steps, 1: odd k-steps
+    const int row = 32 * q + lane;  // tile row = TMEM lane
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * q) << 16);
+    const DecodeConsts dc = make_consts();
+    int wj = 0, a_use = 0;  // a_use: productions into A stage p so far
+    bool ok = true;
+    for (int t = cta; t < args.tiles && ok; t += ncta) {
+      for (int j = 0; j < wstages && ok; ++j) {
+        const int s = wj % kStagesW;
+        const bool landed = mbar_wait(B.w_full + 8 * s, (wj / kStagesW) & 1, abort_flag);
+        if (!__all_sync(0xffffffffu, landed)) {  // warp-uniform verdict
+          ok = false;
+          break;
+        }
+        uint32_t r[36];
+        const uint32_t src = wsm + s * kPackedStageBytes + row * kSuperBytes;
+#pragma unroll
+        for (int i = 0; i < 9; ++i) {
+          const uint4 v = lds128(src + 16 * i);
+          r[4 * i + 0] = v.x;
+          r[4 * i + 1] = v.y;
+          r[4 * i + 2] = v.z;
+          r[4 * i + 3] = v.w;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(B.w_empty + 8 * s);
+        ++wj;
+        // k-steps 4j + p and 4j + p + 2 (blocks 2p, 2p + 1 and 2p + 4, 2p + 5 of
+        // the run) go to A stage p
+        auto one_kstep = [&](auto kk_tag) -> bool {
+          constexpr int KK = decltype(kk_tag)::value;
+          const bool free_stage = mbar_wait(B.a_empty + 8 * p, (a_use & 1) ^ 1, abort_flag);
+          if (!__all_sync(0xffffffffu, free_stage)) return false;
+          tc_fence_after();
+          uint32_t o[32];
+          decode_block_bf16<2 * KK>(r, dc, o);
+          decode_block_bf16<2 * KK + 1>(r, dc, o + 16);
+          tmem_st32(lane_addr + a_col(p), o);
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(B.a_full + 8 * p);
+          ++a_use;
+          return true;
+        };
+        if (p == 0)
+          ok = one_kstep(std::integral_constant<int, 0>{}) &&
+               one_kstep(std::integral_constant<int, 2>{});
+        else
+          ok = one_kstep(std::integral_constant<int, 1>{}) &&
+               one_kstep(std::integral_constant<int, 3>{});
+      }
+    }
+    if (!ok) fail();
+  } else {
+    // ---------------- epilogue
+    const int q = warp & 3;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+    int iter = 0;
+    bool ok = true;
+    for (int t = cta; t < args.tiles && ok; t += ncta, ++iter) {
+      const int b = iter & 1;
+      const int64_t n0 = static_cast<int64_t>(t % args.n_tiles) * kTileRows;
+      const int64_t m0 = static_cast<int64_t>(t / args.n_tiles) * args.bn;
+      const bool done = mbar_wait(B.acc_full + 8 * b, (iter >> 1) & 1, abort_flag);
+      if (!__all_sync(0xffffffffu, done)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int64_t grow = n0 + 32 * q + lane;
+#pragma unroll 1
+      for (int c0 = 0; c0 < args.bn; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_base + acc_col(b) + c0, v);
+        tmem_ld_wait();
+        if (c0 + 32 >= args.bn) {  // the accumulator can be reused once it is read
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(B.acc_empty + 8 * b);
+        }
+        if (grow < args.n) {
+          const int64_t tleft = args.m - (m0 + c0);
+          const int cnt = tleft < 32 ? static_cast<int>(tleft) : 32;
+          if (args.y_bf16) {
+            __nv_bfloat16* yp = static_cast<__nv_bfloat16*>(args.y) + (m0 + c0) * args.ldy + grow;
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (j < cnt) yp[j * args.ldy] = __float2bfloat16_rn(__uint_as_float(v[j]));
+          } else {
+            float* yp = static_cast<float*>(args.y) + (m0 + c0) * args.ldy + grow;
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (j < cnt) yp[j * args.ldy] = __uint_as_float(v[j]);
+          }
+        }
+      }
+    }
+    if (!ok) fail();
   }
 
   tc_fence_before();
@@ -421,21 +492,49 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------ host side
 
-int pick_bn(int64_t m) {
-  if (m <= 16) return 16;
-  if (m <= 32) return 32;
-  if (m <= 64) return 64;
-  if (m <= 128) return 128;
-  if (m <= 192) return 192;
-  if (m <= 256) return 256;
-  const int64_t t192 = (m + 191) / 192 * 192, t256 = (m + 255) / 256 * 256;
-  return t192 < t256 ? 192 : 256;
+int x_stages_for(int bn) {
+  const int avail = kSmemBudget - 1024 /* alignment */ - kStagesW * kPackedStageBytes - kBarBytes;
+  int s = avail / (bn * 128);
+  return s > kMaxXStages ? kMaxXStages : s;
 }
 
-template <int BN>
-cudaError_t launch_bn(const uint8_t* W, int64_t n, int64_t k, const void* X, int64_t m,
-                      int64_t ldx, void* Y, bool y_bf16, int64_t ldy, int32_t* status,
-                      bool pdl, cudaStream_t s) {
+}  // namespace
+
+GemmPlan gemm_plan(int64_t n, int64_t k, int64_t m) {
+  (void)k;
+  GemmPlan p = {};
+  p.n_tiles = (n + kTileRows - 1) / kTileRows;
+  const int64_t g = sm_count();
+  // Pick the token-tile width that finishes in the fewest tile-widths of time:
+  // each tile costs about max(BN, 80) + 32 token-columns (the dequantization
+  // of 128 x K weights bounds narrow tiles; 32 covers the per-tile overhead),
+  // and tiles run in waves of one per SM.
+  int64_t best_cost = -1;
+  for (int bn = 32; bn <= kMaxBN; bn += 32) {
+    const int64_t mt = (m + bn - 1) / bn;
+    const int64_t tiles = p.n_tiles * mt;
+    const int64_t waves = (tiles + g - 1) / g;
+    const int64_t cost = waves * ((bn > 80 ? bn : 80) + 32);
+    if (best_cost < 0 || cost <= best_cost) {
+      best_cost = cost;
+      p.block_n = bn;
+      p.m_tiles = mt;
+    }
+    if (bn >= m) break;
+  }
+  p.splits = 1;
+  p.ws_bytes = 0;
+  return p;
+}
+
+cudaError_t gemm_launch(const GemmPlan& plan, const uint8_t* W, int64_t n, int64_t k,
+                        const void* X, int64_t m, int64_t ldx, void* Y, bool y_bf16,
+                        int64_t ldy, void* workspace, int32_t* status, uint32_t flags,
+                        cudaStream_t s) {
+  (void)workspace;
+  const int64_t tiles = plan.n_tiles * plan.m_tiles;
+  if (tiles > (int64_t(1) << 30)) return cudaErrorNotSupported;
+  const int bn = plan.block_n;
   CUtensorMap tw, tx;
   if (!encode_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, W,
                       static_cast<uint64_t>(k / 32 * kBlockBytes), static_cast<uint64_t>(n),
@@ -444,15 +543,15 @@ cudaError_t launch_bn(const uint8_t* W, int64_t n, int64_t k, const void* X, int
     return cudaErrorInvalidValue;
   if (!encode_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, static_cast<uint64_t>(k),
                       static_cast<uint64_t>(m), static_cast<uint64_t>(ldx * 2), kKStep,
-                      static_cast<uint32_t>(BN), CU_TENSOR_MAP_SWIZZLE_128B))
+                      static_cast<uint32_t>(bn), CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   static bool configured[64] = {false};
   int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN>,
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Smem<BN>::kAlloc);
+                                         kSmemBudget);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
@@ -464,49 +563,22 @@ cudaError_t launch_bn(const uint8_t* W, int64_t n, int64_t k, const void* X, int
   a.y = Y;
   a.status = status;
   a.y_bf16 = y_bf16 ? 1 : 0;
+  a.bn = bn;
+  a.n_tiles = static_cast<int>(plan.n_tiles);
+  a.tiles = static_cast<int>(tiles);
+  a.x_stages = x_stages_for(bn);
+  const int64_t g = sm_count();
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>((n + kTileRows - 1) / kTileRows),
-                     static_cast<unsigned>((m + BN - 1) / BN));
+  cfg.gridDim = dim3(static_cast<unsigned>(tiles < g ? tiles : g));
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = Smem<BN>::kAlloc;
+  cfg.dynamicSmemBytes = kSmemBudget;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN>, tw, tx, a);
-}
-
-}  // namespace
-
-GemmPlan gemm_plan(int64_t n, int64_t k, int64_t m) {
-  GemmPlan p = {};
-  p.block_n = pick_bn(m);
-  p.n_tiles = (n + kTileRows - 1) / kTileRows;
-  p.m_tiles = (m + p.block_n - 1) / p.block_n;
-  p.splits = 1;
-  p.ws_bytes = 0;
-  (void)k;
-  return p;
-}
-
-cudaError_t gemm_launch(const GemmPlan& plan, const uint8_t* W, int64_t n, int64_t k,
-                        const void* X, int64_t m, int64_t ldx, void* Y, bool y_bf16,
-                        int64_t ldy, void* workspace, int32_t* status, uint32_t flags,
-                        cudaStream_t s) {
-  (void)workspace;
-  const bool pdl = (flags & 1u) != 0;
-  if (plan.m_tiles > 65535) return cudaErrorNotSupported;
-  switch (plan.block_n) {
-    case 16: return launch_bn<16>(W, n, k, X, m, ldx, Y, y_bf16, ldy, status, pdl, s);
-    case 32: return launch_bn<32>(W, n, k, X, m, ldx, Y, y_bf16, ldy, status, pdl, s);
-    case 64: return launch_bn<64>(W, n, k, X, m, ldx, Y, y_bf16, ldy, status, pdl, s);
-    case 128: return launch_bn<128>(W, n, k, X, m, ldx, Y, y_bf16, ldy, status, pdl, s);
-    case 192: return launch_bn<192>(W, n, k, X, m, ldx, Y, y_bf16, ldy, status, pdl, s);
-    case 256: return launch_bn<256>(W, n, k, X, m, ldx, Y, y_bf16, ldy, status, pdl, s);
-  }
-  return cudaErrorNotSupported;
+  cfg.numAttrs = (flags & 1u) ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, tw, tx, a);
 }
 
 }  // namespace q4

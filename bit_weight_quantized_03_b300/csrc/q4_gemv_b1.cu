@@ -62,77 +62,6 @@ struct B1Params {
   uint32_t flags;
 };
 
-// w >> 12 computed as the high word of w * 2^20: an integer multiply, issued
-// to the FMA pipe instead of the (busier) ALU pipe.
-__device__ __forceinline__ uint32_t shr12(uint32_t w) { return __umulhi(w, 1u << 20); }
-
-// Loop-invariant decode constants, kept in registers: the exponent bits of
-// 2^(23-p) for the five nibble positions p = 0, 4, 8, 12, 16, and the packed
-// (2^(23-pa) + 8, 2^(23-pb) + 8) bias pairs of the four position pairs used.
-// Written through an opaque move so that each magic OR stays one LOP3 (mask as
-// the immediate, bits from the register) instead of an AND plus an OR.
-struct DecodeConsts {
-  uint32_t bits[5];
-  unsigned long long bias_16_12, bias_8_16, bias_0_8, bias_4_12;
-};
-
-__device__ __forceinline__ uint32_t opaque(uint32_t v) {
-  uint32_t r;
-  asm volatile("mov.b32 %0, %1;" : "=r"(r) : "r"(v));
-  return r;
-}
-
-__device__ __forceinline__ DecodeConsts make_consts() {
-  DecodeConsts c;
-  c.bits[0] = opaque(NibbleMagic<0>::kBits);
-  c.bits[1] = opaque(NibbleMagic<4>::kBits);
-  c.bits[2] = opaque(NibbleMagic<8>::kBits);
-  c.bits[3] = opaque(NibbleMagic<12>::kBits);
-  c.bits[4] = opaque(NibbleMagic<16>::kBits);
-  auto bias = [](float a, float b) {
-    return pack2(__uint_as_float(opaque(__float_as_uint(a))),
-                 __uint_as_float(opaque(__float_as_uint(b))));
-  };
-  c.bias_16_12 = bias(NibbleMagic<16>::kBias, NibbleMagic<12>::kBias);
-  c.bias_8_16 = bias(NibbleMagic<8>::kBias, NibbleMagic<16>::kBias);
-  c.bias_0_8 = bias(NibbleMagic<0>::kBias, NibbleMagic<8>::kBias);
-  c.bias_4_12 = bias(NibbleMagic<4>::kBias, NibbleMagic<12>::kBias);
-  return c;
-}
-
-template <int P>
-__device__ __forceinline__ uint32_t pos_bits(const DecodeConsts& c) {
-  return c.bits[P / 4];
-}
-
-template <int PA, int PB>
-__device__ __forceinline__ unsigned long long pair_bias(const DecodeConsts& c) {
-  if constexpr (PA == 16 && PB == 12) return c.bias_16_12;
-  else if constexpr (PA == 8 && PB == 16) return c.bias_8_16;
-  else if constexpr (PA == 0 && PB == 8) return c.bias_0_8;
-  else return c.bias_4_12;
-}
-
-// (q - 8) for the weight pair whose nibbles sit at bit PA of wa and PB of wb:
-// two LOP3 ((w & 0xF << p) | bits(2^(23-p))) and one packed fp32x2 subtract.
-template <int PA, int PB>
-__device__ __forceinline__ unsigned long long qm8(uint32_t wa, uint32_t wb,
-                                                  const DecodeConsts& c) {
-  static_assert((PA == 16 && PB == 12) || (PA == 8 && PB == 16) || (PA == 0 && PB == 8) ||
-                    (PA == 4 && PB == 12),
-                "position pair without a bias constant");
-  unsigned long long r;
-  asm("{\n\t.reg .b32 lo, hi;\n\t"
-      "lop3.b32 lo, %1, %3, %4, 0xEA;\n\t"
-      "lop3.b32 hi, %2, %5, %6, 0xEA;\n\t"
-      "mov.b64 %0, {lo, hi};\n\t"
-      "sub.rn.f32x2 %0, %0, %7;\n\t}"
-      : "=l"(r)
-      : "r"(wa), "r"(wb), "n"(NibbleMagic<PA>::kMask), "r"(pos_bits<PA>(c)),
-        "n"(NibbleMagic<PB>::kMask), "r"(pos_bits<PB>(c)), "l"(pair_bias<PA, PB>(c)));
-  return r;
-}
-
 // Dot product of block BLK (0 or 1) of a 36-byte block pair r[9] (only the
 // words of that block are read) with its 16 activation pairs xb: returns sum_e (q_e - 8) * x_e as an fp32
 // pair (even and odd elements) and the block's scale in d.

@@ -162,22 +162,27 @@ class EncoderStack:
     def launches_per_pass(self) -> int:
         return 4 * self.layers
 
-    def _layer(self, l, x_in, stream):
+    def flops(self, frames: int) -> int:
+        return 2 * frames * self.layers * sum(n * k for n, k in self.shapes.values())
+
+    def _layer(self, l, x_in, m, stream):
         W, D, F = self.W[l], self.DIM, self.FFN
-        q4_gemm(W["qkv"], 3 * D, D, x_in, Y=self.y_qkv, workspace=self.ws, flags=FLAG_PDL,
+        q4_gemm(W["qkv"], 3 * D, D, x_in, Y=self.y_qkv[:m], workspace=self.ws, flags=FLAG_PDL,
                 stream=stream)
-        q4_gemm(W["out"], D, D, self.y_qkv[:, :D], Y=self.y_out, workspace=self.ws,
+        q4_gemm(W["out"], D, D, self.y_qkv[:m, :D], Y=self.y_out[:m], workspace=self.ws,
                 flags=FLAG_PDL, stream=stream)
-        q4_gemm(W["up"], F, D, self.y_out, Y=self.y_up, workspace=self.ws, flags=FLAG_PDL,
-                stream=stream)
-        q4_gemm(W["down"], D, F, self.y_up, Y=self.x, workspace=self.ws, flags=FLAG_PDL,
+        q4_gemm(W["up"], F, D, self.y_out[:m], Y=self.y_up[:m], workspace=self.ws,
+                flags=FLAG_PDL, stream=stream)
+        q4_gemm(W["down"], D, F, self.y_up[:m], Y=self.x[:m], workspace=self.ws, flags=FLAG_PDL,
                 stream=stream)
 
     def forward(self, x_in, stream=None):
-        self._layer(0, x_in, stream)
+        """x_in [m, 1280] bf16 with m <= frames -> self.x[:m]."""
+        m = x_in.shape[0]
+        self._layer(0, x_in, m, stream)
         for l in range(1, self.layers):
-            self._layer(l, self.x, stream)
-        return self.x
+            self._layer(l, self.x[:m], m, stream)
+        return self.x[:m]
 
     def capture(self, x_in, stream, passes: int = 1):
         torch = self.torch
