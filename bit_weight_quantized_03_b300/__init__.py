@@ -14,14 +14,14 @@ per token).
 """
 from __future__ import annotations
 
-from ._lib import (BF16, BLOCK_BYTES, BLOCK_ELEMS, ERR_CUDA, ERR_ID_OUT_OF_RANGE,  # noqa: F401
+from ._lib import (BF16, BLOCK_BYTES, CHAIN_MAX_STAGES, GemvStage, BLOCK_ELEMS, ERR_CUDA, ERR_ID_OUT_OF_RANGE,  # noqa: F401
                    ERR_INVALID_ARG, ERR_MISALIGNED, ERR_NONFINITE, ERR_TIMEOUT,
                    ERR_UNSUPPORTED_SHAPE, ERR_WORKSPACE, F32, FLAG_PDL, FLAG_TEST_STALL,
                    GEMV_MAX_M, GEMV_NOALLOC_SCRATCH_BYTES, OK, Q4Error, check, lib,
                    status_string)
 
 __all__ = [
-    "q4_quantize", "q4_dequant_rows", "q4_gemv", "q4_gemv_noalloc", "q4_gemm", "q4_embed_gather", "q4_linear",
+    "q4_quantize", "q4_dequant_rows", "q4_gemv", "q4_gemv_noalloc", "q4_gemv_chain", "q4_gemm", "q4_embed_gather", "q4_linear",
     "q4_gemv_workspace_bytes", "q4_gemm_workspace_bytes", "q4_linear_workspace_bytes",
     "q4_linear_crossover_m", "Workspace", "Q4Error", "lib", "packed_bytes",
 ]
@@ -165,6 +165,27 @@ def q4_gemv_noalloc(W, n: int, k: int, x, y=None, status=None, flags: int = 0, s
     check(lib().q4_gemv_noalloc(_ptr(W), n, k, _ptr(x), m, ldx, _ptr(y), ldy, _ptr(status),
                                 flags, _stream(stream)), "q4_gemv_noalloc")
     return y
+
+
+def _chain_array(stages):
+    arr = (GemvStage * len(stages))()
+    for i, (W, n, k, x, y) in enumerate(stages):
+        arr[i].W, arr[i].n, arr[i].k = _ptr(W), n, k
+        arr[i].x, arr[i].y = _ptr(x), _ptr(y)
+    return arr
+
+
+def q4_gemv_chain_workspace_bytes(stages) -> int:
+    return int(lib().q4_gemv_chain_workspace_bytes(_chain_array(stages), len(stages)))
+
+
+def q4_gemv_chain(stages, workspace=None, status=None, flags: int = 0, stream=None):
+    """Run links (W, n, k, x, y) in order, y = W x each (batch 1, fp32), in one
+    launch; x may be a slice of an earlier link's y (torch views)."""
+    arr = _chain_array(stages)
+    buf, nbytes = _workspace(workspace, int(lib().q4_gemv_chain_workspace_bytes(arr, len(stages))))
+    check(lib().q4_gemv_chain(arr, len(stages), _ptr(buf), nbytes, _ptr(status), flags,
+                              _stream(stream)), "q4_gemv_chain")
 
 
 def q4_gemm(W, n: int, k: int, X, Y=None, y_dtype=None, workspace=None, status=None,

@@ -29,6 +29,14 @@ GEMV_NOALLOC_SCRATCH_BYTES = 4 << 20
 BLOCK_ELEMS = 32
 BLOCK_BYTES = 18
 
+class GemvStage(ctypes.Structure):
+    """struct q4_gemv_stage of include/q4.h."""
+    _fields_ = [("W", ctypes.c_void_p), ("n", ctypes.c_int64), ("k", ctypes.c_int64),
+                ("x", ctypes.c_void_p), ("y", ctypes.c_void_p)]
+
+
+CHAIN_MAX_STAGES = 128
+
 # Every symbol include/q4.h declares, with its ctypes signature.
 _vp, _i64, _sz, _u32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t, ctypes.c_uint32
 _st = ctypes.c_int
@@ -38,6 +46,8 @@ SIGNATURES = {
     "q4_gemv": (_st, [_vp, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _vp, _sz, _vp, _u32, _vp]),
     "q4_gemv_workspace_bytes": (_sz, [_i64, _i64, _i64]),
     "q4_gemv_noalloc": (_st, [_vp, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _vp, _u32, _vp]),
+    "q4_gemv_chain": (_st, [ctypes.POINTER(GemvStage), ctypes.c_int32, _vp, _sz, _vp, _u32, _vp]),
+    "q4_gemv_chain_workspace_bytes": (_sz, [ctypes.POINTER(GemvStage), ctypes.c_int32]),
     "q4_gemm": (_st, [_vp, _i64, _i64, _vp, _i64, _i64, _vp, ctypes.c_int, _i64, _vp, _sz, _vp,
                       _u32, _vp]),
     "q4_gemm_workspace_bytes": (_sz, [_i64, _i64, _i64]),

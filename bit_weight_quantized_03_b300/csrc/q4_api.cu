@@ -3,6 +3,7 @@
 // the batch-size crossover of q4_linear, and the kernel launches.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "../../include/q4.h"
@@ -141,6 +142,93 @@ q4_status q4_embed_gather(const void* table, int64_t vocab, int64_t k, const int
   if (!aligned(ids, 4) || !aligned(out, 16)) return Q4_ERR_MISALIGNED;
   return from_cuda(q4::embed_gather_launch(static_cast<const uint8_t*>(table), vocab, k, ids, n_ids,
                                            out, status_dev, reinterpret_cast<cudaStream_t>(s)));
+}
+
+}  // extern "C"
+
+namespace {
+
+// Validates a chain and fills the kernel parameters (except the pointers that
+// come from the workspace).  Returns the workspace the chain needs in *ws.
+q4_status plan_chain(const q4_gemv_stage* st, int32_t ns, q4::ChainParams* cp, size_t* ws) {
+  if (st == nullptr || ns < 1 || ns > Q4_CHAIN_MAX_STAGES || ns > q4::kMaxChain)
+    return Q4_ERR_INVALID_ARG;
+  const int ctas = q4::sm_count();
+  const int64_t kmax = q4::gemv_chain_max_k();
+  int64_t max_pn = 0;
+  for (int32_t s = 0; s < ns; ++s) {
+    const q4_gemv_stage& a = st[s];
+    q4_status e = check_matrix(a.W, a.n, a.k);
+    if (e != Q4_OK) return e;
+    if (a.x == nullptr || a.y == nullptr) return Q4_ERR_INVALID_ARG;
+    if (a.k % 256 != 0 || a.k > kmax || a.n % 4 != 0 || a.n > (int64_t(1) << 30))
+      return Q4_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(a.x, 16) || !aligned(a.y, 4)) return Q4_ERR_MISALIGNED;
+    const int64_t groups = (a.n + 31) / 32, nsb = a.k / 256;
+    const int p = q4::gemv_chain_split(groups, nsb, ctas);
+    if (p == 0) return Q4_ERR_UNSUPPORTED_SHAPE;
+    max_pn = std::max<int64_t>(max_pn, p * a.n);
+    // Links behave as if run one after another.  x_s overlapping the previous
+    // link's y is taken from that link's partial sums (the buffer itself is
+    // written while link s starts), so it must lie inside it, on a multiple
+    // of 4 floats; any other x is read from memory as it stands then.
+    int32_t x_off = -1;
+    if (s > 0) {
+      const uintptr_t xb = reinterpret_cast<uintptr_t>(a.x), xe = xb + 4 * a.k;
+      const uintptr_t yb = reinterpret_cast<uintptr_t>(st[s - 1].y), ye = yb + 4 * st[s - 1].n;
+      if (xb < ye && yb < xe) {
+        if (xb < yb || xe > ye || (xb - yb) % 16 != 0) return Q4_ERR_INVALID_ARG;
+        x_off = static_cast<int32_t>((xb - yb) / 4);
+      }
+    }
+    if (cp != nullptr) {
+      q4::ChainStage& c = cp->st[s];
+      c.x = a.x;
+      c.y = a.y;
+      c.n = static_cast<int32_t>(a.n);
+      c.nsb = static_cast<int32_t>(nsb);
+      c.groups = static_cast<int32_t>(groups);
+      c.P = p;
+      c.x_off = x_off;
+      c.reserved = 0;
+      const uint64_t rowbytes = static_cast<uint64_t>(a.k / 32 * Q4_BLOCK_BYTES);
+      if (!q4::encode_tmap_2d(&cp->tmap[s], CU_TENSOR_MAP_DATA_TYPE_UINT8, a.W, rowbytes,
+                              static_cast<uint64_t>(a.n), rowbytes, 144, 32,
+                              CU_TENSOR_MAP_SWIZZLE_NONE))
+        return Q4_ERR_CUDA;
+    }
+  }
+  const size_t part = (static_cast<size_t>(max_pn) * 4 + 255) / 256 * 256;
+  *ws = 256 + 2 * part;
+  if (cp != nullptr) cp->n_stages = ns;
+  return Q4_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t q4_gemv_chain_workspace_bytes(const q4_gemv_stage* stages, int32_t n_stages) {
+  size_t ws = 0;
+  return plan_chain(stages, n_stages, nullptr, &ws) == Q4_OK ? ws : 0;
+}
+
+q4_status q4_gemv_chain(const q4_gemv_stage* stages, int32_t n_stages, void* workspace,
+                        size_t ws_bytes, int32_t* status_dev, uint32_t flags, q4_stream_t s) {
+  static thread_local q4::ChainParams cp;  // ~21 KB: kept off the stack
+  size_t need = 0;
+  q4_status st = plan_chain(stages, n_stages, &cp, &need);
+  if (st != Q4_OK) return st;
+  if (workspace == nullptr || ws_bytes < need) return Q4_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return Q4_ERR_MISALIGNED;
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  const size_t part = (need - 256) / 2;
+  cp.done = reinterpret_cast<int32_t*>(w);
+  cp.part[0] = reinterpret_cast<float*>(w + 256);
+  cp.part[1] = reinterpret_cast<float*>(w + 256 + part);
+  cp.status = status_dev;
+  cp.flags = flags;
+  return from_cuda(q4::gemv_chain_launch(cp, reinterpret_cast<cudaStream_t>(s)));
 }
 
 int64_t q4_linear_crossover_m(int64_t n, int64_t k) {

@@ -33,22 +33,20 @@
 //   * Row groups split between warps are finished deterministically: partial
 //     row sums go to the workspace, the last warp to arrive (atomic counter)
 //     adds them in warp order, zeroes them and resets the counter.
-#include "q4_device.cuh"
+#include "q4_gemv_tile.cuh"
 
 namespace q4 {
 namespace {
+
+using tile::unit_dot;
+using tile::xpad_floats;
+using tile::xpad_index;
 
 constexpr int kWarps = 16;                    // warps per CTA, one CTA per SM
 constexpr int kStages = 2;                    // ring slots per warp
 constexpr int kSlotBytes = 32 * kSuperBytes;  // 32 rows x 144 B
 constexpr int kRingBytes = kWarps * kStages * kSlotBytes;
 constexpr int kMaxSmem = 226 * 1024;  // dynamic part; the static barriers need the rest
-
-// x is staged once per CTA in shared memory, with 16 bytes of padding after
-// every 64 floats, so that the four block pairs a warp reads at once (256 B
-// apart in x) fall into different banks.
-__host__ __device__ constexpr int64_t xpad_floats(int64_t k) { return k + k / 64 * 4; }
-__device__ __forceinline__ int xpad_index(int e) { return e + (e >> 6) * 4; }
 
 struct B1Params {
   const uint8_t* W;
@@ -62,69 +60,11 @@ struct B1Params {
   uint32_t flags;
 };
 
-// Dot product of block BLK (0 or 1) of a 36-byte block pair r[9] (only the
-// words of that block are read) with its 16 activation pairs xb: returns sum_e (q_e - 8) * x_e as an fp32
-// pair (even and odd elements) and the block's scale in d.
-//   BLK 0: d = low half of r[0]; qs[0..1] high half of r[0], qs[2..13] in
-//          r[1..3], qs[14..15] low half of r[4].
-//   BLK 1: d = high half of r[4]; qs[0..15] in r[5..8].
-// Byte c of qs holds element c (low nibble) and element c + 16 (high nibble).
-template <int BLK>
-__device__ __forceinline__ unsigned long long block_dot(const uint32_t (&r)[9],
-                                                        const unsigned long long (&xb)[16],
-                                                        const DecodeConsts& c, float& d) {
-  unsigned long long acc;
-  if constexpr (BLK == 0) {
-    d = half_bits_to_float(r[0]);
-    {
-      const uint32_t w = r[0], t = shr12(w);
-      acc = fmul2(qm8<16, 12>(w, t, c), xb[0]);          // elements 0, 1
-      acc = ffma2(qm8<8, 16>(t, t, c), xb[8], acc);      // 16, 17
-    }
-#pragma unroll
-    for (int i = 0; i < 3; ++i) {
-      const uint32_t w = r[1 + i], t = shr12(w);      // qs[2+4i .. 5+4i]
-      acc = ffma2(qm8<0, 8>(w, w, c), xb[1 + 2 * i], acc);    // 2+4i, 3+4i
-      acc = ffma2(qm8<16, 12>(w, t, c), xb[2 + 2 * i], acc);  // 4+4i, 5+4i
-      acc = ffma2(qm8<4, 12>(w, w, c), xb[9 + 2 * i], acc);   // 18+4i, 19+4i
-      acc = ffma2(qm8<8, 16>(t, t, c), xb[10 + 2 * i], acc);  // 20+4i, 21+4i
-    }
-    {
-      const uint32_t w = r[4];
-      acc = ffma2(qm8<0, 8>(w, w, c), xb[7], acc);   // 14, 15
-      acc = ffma2(qm8<4, 12>(w, w, c), xb[15], acc); // 30, 31
-    }
-  } else {
-    d = half_bits_to_float(r[4] >> 16);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t w = r[5 + i], t = shr12(w);      // qs[4i .. 4i+3]
-      const unsigned long long a = qm8<0, 8>(w, w, c);   // 4i, 4i+1
-      acc = i == 0 ? fmul2(a, xb[0]) : ffma2(a, xb[2 * i], acc);
-      acc = ffma2(qm8<16, 12>(w, t, c), xb[2 * i + 1], acc);  // 4i+2, 4i+3
-      acc = ffma2(qm8<4, 12>(w, w, c), xb[8 + 2 * i], acc);   // 4i+16, 4i+17
-      acc = ffma2(qm8<8, 16>(t, t, c), xb[9 + 2 * i], acc);   // 4i+18, 4i+19
-    }
-  }
-  return acc;
-}
-
-__device__ __forceinline__ void lds_v2u64(uint32_t addr, unsigned long long& a,
-                                          unsigned long long& b) {
-  asm volatile("ld.shared.v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "r"(addr));
-}
-
 __device__ __forceinline__ int atomic_add_acq_rel_gpu(int32_t* p, int v) {
   int old;
   asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
                : "memory");
   return old;
-}
-
-__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
-  return v;
 }
 
 // First unit of warp i when `units` units are cut into `warps` contiguous
@@ -239,25 +179,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
       ok = false;
       break;
     }
-    const uint32_t src = slots + slot * kSlotBytes + rr * kSuperBytes + 36 * j;
-    const int xe = static_cast<int>(sb * kSuperElems) + 64 * j;  // first element of the pair
-#pragma unroll
-    for (int b = 0; b < 2; ++b) {
-      unsigned long long xb[16];
-      const uint32_t xa = xs + 4 * xpad_index(xe + 32 * b);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) lds_v2u64(xa + 16 * i, xb[2 * i], xb[2 * i + 1]);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        uint32_t r[9];
-#pragma unroll
-        for (int w = 0; w < 5; ++w)
-          r[4 * b + w] = lds32(src + i * 8 * kSuperBytes + 4 * (4 * b + w));
-        float d;
-        const f2 a = unpack2(b == 0 ? block_dot<0>(r, xb, dc, d) : block_dot<1>(r, xb, dc, d));
-        yv[i] = fmaf(a.x + a.y, d, yv[i]);
-      }
-    }
+    unit_dot(slots + slot * kSlotBytes, xs, static_cast<int>(sb), j, rr, dc, yv);
     __syncwarp();
     fence_proxy_async_smem();
     if (issued < nunits) issue_next();

@@ -2,6 +2,7 @@
 // and the kernel files.  Not part of the public interface (that is include/q4.h).
 #pragma once
 
+#include <algorithm>
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
@@ -45,6 +46,33 @@ bool gemv_b1_supports(int64_t k);
 cudaError_t gemv_b1_launch(const uint8_t* W, int64_t n, int64_t k, const float* x, float* y,
                            int32_t* counters, float* partials, int64_t units, int64_t warps,
                            int32_t* status, uint32_t flags, cudaStream_t s);
+
+// --------------------------------------------------------------- GEMV chain
+constexpr int kMaxChain = 128;      // links per launch
+constexpr int kMaxChainItems = 8;   // (row group, K-split) items per CTA per link
+
+struct ChainStage {
+  const float* x;       // external input (x_off < 0)
+  float* y;             // output, written once the next link starts
+  int32_t n, nsb;       // rows, 256-wide slices of k
+  int32_t groups, P;    // 32-row groups, K-splits
+  int32_t x_off;        // >= 0: x = y of the previous link from this element
+  int32_t reserved;
+};
+
+struct ChainParams {
+  CUtensorMap tmap[kMaxChain];  // per link: the packed matrix, box 144 B x 32 rows
+  ChainStage st[kMaxChain];
+  int32_t n_stages;
+  int32_t* done;                // barrier counter (workspace, zero between launches)
+  float* part[2];               // per-link partial sums [P][n], alternating buffers
+  int32_t* status;
+  uint32_t flags;
+};
+
+int64_t gemv_chain_max_k();
+int gemv_chain_split(int64_t groups, int64_t nsb, int ctas);  // 0: too many rows
+cudaError_t gemv_chain_launch(ChainParams& params, cudaStream_t s);
 
 // --------------------------------------------------------------- GEMM (tcgen05)
 struct GemmPlan {

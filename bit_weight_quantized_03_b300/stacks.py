@@ -17,14 +17,16 @@ chain of dependent products that a real decode step has.
 Layout in HBM: per decoder layer three row-concatenated matrices that share an
 input -- Wqkv = [wq; wk; wv] (6144 x 3072), W13 = [w1; w3] (18432 x 3072) --
 plus wo (3072 x 4096) and w2 (3072 x 9216), each a contiguous run of Q4_0 rows.
-A decode step is 4 dependent GEMV launches per layer (104 per step) with
-programmatic dependent launch between them, captured in a CUDA graph.
+A decode step is 4 dependent products per layer (104 per step), run either as
+one q4_gemv_chain launch (persistent, the weight stream never stops between
+products) or as 104 q4_gemv launches with programmatic dependent launch
+between them; either is captured in a CUDA graph.
 """
 from __future__ import annotations
 
 import synth
 
-from . import FLAG_PDL, Workspace, q4_gemm, q4_gemv, q4_quantize
+from . import FLAG_PDL, Workspace, q4_gemm, q4_gemv, q4_gemv_chain, q4_quantize
 
 
 def _quantize_rows(parts, k, device, torch):
@@ -74,6 +76,9 @@ class DecoderStack:
         for name, (n, k) in self.shapes.items():  # size the shared workspace once
             from . import q4_gemv_workspace_bytes
             self.ws.get(q4_gemv_workspace_bytes(n, k, 1))
+        from . import q4_gemv_chain_workspace_bytes
+        self.chain_ws = Workspace(self.device)
+        self.chain_ws.get(q4_gemv_chain_workspace_bytes(self.links(self.x)))
         self.graphs = {}
 
     # bytes the method must move per decode step (weights once + activations)
@@ -100,23 +105,40 @@ class DecoderStack:
         q4_gemv(W["w2"], h, self.FFN, self.y_13[:, :self.FFN], y=self.x, workspace=self.ws,
                 flags=FLAG_PDL, stream=stream)
 
-    def step(self, x_in, stream=None):
-        """One decode step on the device: x_in [1, 3072] fp32 -> self.x [1, 3072]."""
+    def links(self, x_in):
+        """The step's 104 products as chain links (W, n, k, x, y), in order."""
+        H, Q, F = self.HIDDEN, self.QDIM, self.FFN
+        out = []
+        for l in range(self.layers):
+            W = self.W[l]
+            out.append((W["qkv"], Q + 2 * self.KVDIM, H, x_in if l == 0 else self.x, self.y_qkv))
+            out.append((W["wo"], H, Q, self.y_qkv[:, :Q], self.y_o))
+            out.append((W["w13"], 2 * F, H, self.y_o, self.y_13))
+            out.append((W["w2"], H, F, self.y_13[:, :F], self.x))
+        return out
+
+    def step(self, x_in, stream=None, chain: bool = False):
+        """One decode step on the device: x_in [1, 3072] fp32 -> self.x [1, 3072].
+        chain=True runs the 104 products as one q4_gemv_chain launch; otherwise
+        one q4_gemv launch each (programmatic dependent launch between them)."""
+        if chain:
+            q4_gemv_chain(self.links(x_in), workspace=self.chain_ws, stream=stream)
+            return self.x
         self._layer(0, x_in, stream)
         for l in range(1, self.layers):
             self._layer(l, self.x, stream)
         return self.x
 
-    def capture(self, inputs, stream):
+    def capture(self, inputs, stream, chain: bool = False):
         """CUDA graph of len(inputs) consecutive steps, step i reading inputs[i]."""
         torch = self.torch
         g = torch.cuda.CUDAGraph()
         with torch.cuda.stream(stream):
-            self.step(inputs[0], stream)  # warm the path outside capture
+            self.step(inputs[0], stream, chain=chain)  # warm the path outside capture
             stream.synchronize()
             with torch.cuda.graph(g, stream=stream):
                 for x_in in inputs:
-                    self.step(x_in, stream)
+                    self.step(x_in, stream, chain=chain)
         return g
 
 

@@ -141,6 +141,39 @@ q4_status q4_gemv_noalloc(const void* W, int64_t n, int64_t k, const float* x, i
                           int64_t ldx, float* y, int64_t ldy, int32_t* status_dev,
                           uint32_t flags, q4_stream_t s);
 
+/* One link of a chain of batch-1 products (q4_gemv_chain). */
+typedef struct q4_gemv_stage {
+  const void* W;  /* [n rows of k/32 blocks], 16-byte aligned */
+  int64_t n;      /* rows; n % 4 == 0 */
+  int64_t k;      /* k % 256 == 0, k <= the kernel's shared-memory limit (15872) */
+  const float* x; /* [k] fp32, 16-byte aligned; may point into the previous link's y */
+  float* y;       /* [n] fp32, 4-byte aligned */
+} q4_gemv_stage;
+
+#define Q4_CHAIN_MAX_STAGES 128
+
+/* A decode step's chain of dependent batch-1 products in one launch:
+ *   for s = 0 .. n_stages-1 in order:  y_s[r] = sum_j w^_s[r][j] * x_s[j]
+ * with the results of running the links one after another: x_s may be (a
+ * slice of) any earlier y_t, and buffers may be reused by later links.  The
+ * decoder of the Voxtral Mini 4B Realtime port ("Arquitectura": 26 layers,
+ * hidden 3072, GQA 32Q/8KV) runs its per-token linears as such a chain, each
+ * reading the previous one's output.  Each y_s is within 1e-4 * sum_j |w^ x|
+ * of the exact product of the x_s it read, with a fixed summation order.
+ *   stages     host array of n_stages links (1 <= n_stages <= 128); read during
+ *              the call only.  An x_s that overlaps y_{s-1} must lie inside it
+ *              and start on a multiple of 4 floats (else Q4_ERR_INVALID_ARG).
+ *   workspace  q4_gemv_chain_workspace_bytes() bytes, 256-byte aligned, zero
+ *              before the first call; every call that ends without a device
+ *              error leaves its counter at zero again.
+ * The launch is cooperative (one CTA per SM, all resident); it fails with
+ * Q4_ERR_CUDA if the GPU cannot hold every CTA at once.  A row count so
+ * large that a link would give one SM more than 8 x 32-row groups returns
+ * Q4_ERR_UNSUPPORTED_SHAPE. */
+q4_status q4_gemv_chain(const q4_gemv_stage* stages, int32_t n_stages, void* workspace,
+                        size_t ws_bytes, int32_t* status_dev, uint32_t flags, q4_stream_t s);
+size_t q4_gemv_chain_workspace_bytes(const q4_gemv_stage* stages, int32_t n_stages);
+
 /* Prefill / audio-encoder product on the tensor cores:
  *   Y[i][r] = sum_j bf16(w^[r][j]) * X[i][j]   (fp32 accumulation)
  * for the 32-layer, 1280-wide encoder and prefill ("Arquitectura"); error within
