@@ -221,7 +221,24 @@ struct GemmArgs {
   int n_tiles;    // tiles along the weight rows
   int tiles;      // n_tiles x token tiles
   int x_stages;   // X ring depth
+  int splits;     // K-splits per tile (work items = tiles x splits)
+  int32_t* counters;  // [tiles] arrivals per tile (splits > 1), zero between calls
+  float* partials;    // [splits][m][n] fp32 (splits > 1)
 };
+
+// Work item w: tile w / splits, K-split w % splits, which covers 256-wide
+// weight stages [j0, j1).
+struct Item {
+  int tile, split, j0, j1;
+};
+__device__ __forceinline__ Item item_of(int w, int splits, int wstages) {
+  Item it;
+  it.tile = w / splits;
+  it.split = w - it.tile * splits;
+  it.j0 = wstages * it.split / splits;
+  it.j1 = wstages * (it.split + 1) / splits;
+  return it;
+}
 
 struct Bars {
   uint32_t w_full, w_empty, x_full, x_empty, a_full, a_empty, acc_full, acc_empty, drain;
@@ -249,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   B.acc_full = B.a_empty + 8 * kAStages;
   B.acc_empty = B.acc_full + 16;
   B.drain = B.acc_empty + 16;
-  const uint32_t misc = B.drain + 8;
+  const uint32_t misc = B.drain + 8;  // tmem slot, abort flag, last-split flag
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gbase + (misc - base));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + (misc - base) + 4);
 
@@ -302,10 +319,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---------------- TMA producer
       int wj = 0, xk = 0;
       bool ok = true;
-      for (int t = cta; t < args.tiles && ok; t += ncta) {
-        const int32_t n0 = (t % args.n_tiles) * kTileRows;
-        const int32_t m0 = (t / args.n_tiles) * args.bn;
-        for (int j = 0; j < wstages && ok; ++j) {
+      for (int w = cta; w < args.tiles * args.splits && ok; w += ncta) {
+        const Item it = item_of(w, args.splits, wstages);
+        const int32_t n0 = (it.tile % args.n_tiles) * kTileRows;
+        const int32_t m0 = (it.tile / args.n_tiles) * args.bn;
+        for (int j = it.j0; j < it.j1 && ok; ++j) {
           const int s = wj % kStagesW;
           if (!mbar_wait(B.w_empty + 8 * s, ((wj / kStagesW) & 1) ^ 1, abort_flag)) {
             ok = false;
@@ -343,14 +361,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       int xk = 0, iter = 0;
       int a_use0 = 0, a_use1 = 0;  // completed uses of A stage 0 / 1
       bool ok = true, any = false;
-      for (int t = cta; t < args.tiles && ok; t += ncta, ++iter) {
+      for (int w = cta; w < args.tiles * args.splits && ok; w += ncta, ++iter) {
+        const Item it = item_of(w, args.splits, wstages);
         const int b = iter & 1;
         if (!mbar_wait(B.acc_empty + 8 * b, ((iter >> 1) & 1) ^ 1, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        for (int ks = 0; ks < ksteps; ++ks) {
+        for (int ks = 4 * it.j0; ks < 4 * it.j1; ++ks) {
           const int p = ks & 1, s2 = xk % nx;
           const int use = p ? a_use1 : a_use0;
           if (!mbar_wait(B.a_full + 8 * p, use & 1, abort_flag) ||
@@ -363,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < kKStep / 16; ++kk)
             umma_ts_bf16(tmem + acc_col(b), tmem + a_col(p) + 8 * kk, bdesc + 2 * kk, idesc,
-                         (ks | kk) != 0);
+                         (ks != 4 * it.j0 || kk != 0) ? 1u : 0u);
           any = true;
           umma_commit(B.x_empty + 8 * s2);
           umma_commit(B.a_empty + 8 * p);
@@ -387,8 +406,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const DecodeConsts dc = make_consts();
     int wj = 0, a_use = 0;  // a_use: productions into A stage p so far
     bool ok = true;
-    for (int t = cta; t < args.tiles && ok; t += ncta) {
-      for (int j = 0; j < wstages && ok; ++j) {
+    for (int w = cta; w < args.tiles * args.splits && ok; w += ncta) {
+      const Item it = item_of(w, args.splits, wstages);
+      for (int j = it.j0; j < it.j1 && ok; ++j) {
         const int s = wj % kStagesW;
         const bool landed = mbar_wait(B.w_full + 8 * s, (wj / kStagesW) & 1, abort_flag);
         if (!__all_sync(0xffffffffu, landed)) {  // warp-uniform verdict
@@ -441,7 +461,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
     int iter = 0;
     bool ok = true;
-    for (int t = cta; t < args.tiles && ok; t += ncta, ++iter) {
+    volatile int* last_flag = abort_flag + 1;  // set by the epilogue's counter thread
+    for (int w = cta; w < args.tiles * args.splits && ok; w += ncta, ++iter) {
+      const Item it = item_of(w, args.splits, wstages);
+      const int t = it.tile;
       const int b = iter & 1;
       const int64_t n0 = static_cast<int64_t>(t % args.n_tiles) * kTileRows;
       const int64_t m0 = static_cast<int64_t>(t / args.n_tiles) * args.bn;
@@ -452,6 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const int64_t grow = n0 + 32 * q + lane;
+      const bool split = args.splits > 1;
 #pragma unroll 1
       for (int c0 = 0; c0 < args.bn; c0 += 32) {
         uint32_t v[32];
@@ -465,7 +489,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (grow < args.n) {
           const int64_t tleft = args.m - (m0 + c0);
           const int cnt = tleft < 32 ? static_cast<int>(tleft) : 32;
-          if (args.y_bf16) {
+          if (split) {  // this K-split's partial tile, fp32
+            float* pp = args.partials + (static_cast<int64_t>(it.split) * args.m + m0 + c0) *
+                                            args.n + grow;
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (j < cnt) __stcg(pp + j * args.n, __uint_as_float(v[j]));
+          } else if (args.y_bf16) {
             __nv_bfloat16* yp = static_cast<__nv_bfloat16*>(args.y) + (m0 + c0) * args.ldy + grow;
 #pragma unroll
             for (int j = 0; j < 32; ++j)
@@ -477,6 +507,50 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (j < cnt) yp[j * args.ldy] = __uint_as_float(v[j]);
           }
         }
+      }
+      if (split) {
+        // The last K-split of the tile to arrive adds the partials in split
+        // order (deterministic), writes Y and puts the counter back to zero.
+        asm volatile("bar.sync 1, 128;" ::: "memory");  // the 4 epilogue warps
+        if (warp == 10 && lane == 0) {
+          __threadfence();
+          const int old = atomicAdd(args.counters + t, 1);
+          *last_flag = old == args.splits - 1;
+          if (old == args.splits - 1) args.counters[t] = 0;
+          __threadfence();
+        }
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        if (*last_flag && grow < args.n) {
+          const int64_t tleft = args.m - m0;
+          const int cnt = tleft < args.bn ? static_cast<int>(tleft) : args.bn;
+          const int64_t split_stride = args.m * args.n;
+          for (int c = 0; c < cnt; c += 4) {  // four tokens at a time: independent loads
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            const float* pp = args.partials + (m0 + c) * args.n + grow;
+            for (int sp = 0; sp < args.splits; ++sp) {
+#pragma unroll
+              for (int u = 0; u < 4; ++u)
+                if (c + u < cnt) acc[u] += __ldcg(pp + sp * split_stride + u * args.n);
+            }
+            // the workspace goes back to all-zero, as every call leaves it
+            for (int sp = 0; sp < args.splits; ++sp) {
+#pragma unroll
+              for (int u = 0; u < 4; ++u)
+                if (c + u < cnt) __stcg(const_cast<float*>(pp) + sp * split_stride + u * args.n, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              if (c + u >= cnt) break;
+              const int64_t tok = m0 + c + u;
+              if (args.y_bf16)
+                static_cast<__nv_bfloat16*>(args.y)[tok * args.ldy + grow] =
+                    __float2bfloat16_rn(acc[u]);
+              else
+                static_cast<float*>(args.y)[tok * args.ldy + grow] = acc[u];
+            }
+          }
+        }
+        asm volatile("bar.sync 1, 128;" ::: "memory");  // last_flag is reused next item
       }
     }
     if (!ok) fail();
@@ -501,7 +575,6 @@ int x_stages_for(int bn) {
 }  // namespace
 
 GemmPlan gemm_plan(int64_t n, int64_t k, int64_t m) {
-  (void)k;
   GemmPlan p = {};
   p.n_tiles = (n + kTileRows - 1) / kTileRows;
   const int64_t g = sm_count();
@@ -522,8 +595,21 @@ GemmPlan gemm_plan(int64_t n, int64_t k, int64_t m) {
     }
     if (bn >= m) break;
   }
+  // Too few tiles for the SMs (small M): split K, in 256-weight stages, so that
+  // tiles x splits fill about one wave; partial tiles are added in the epilogue.
   p.splits = 1;
+  const int64_t tiles = p.n_tiles * p.m_tiles, wstages = k / 256;
+  if (tiles * 2 <= g) {
+    int64_t sp = g / tiles;
+    if (sp > wstages) sp = wstages;
+    if (sp > 16) sp = 16;
+    p.splits = sp > 1 ? sp : 1;
+  }
   p.ws_bytes = 0;
+  if (p.splits > 1) {
+    const size_t cnt = (static_cast<size_t>(tiles) * 4 + 255) / 256 * 256;
+    p.ws_bytes = cnt + static_cast<size_t>(p.splits) * m * n * 4;
+  }
   return p;
 }
 
@@ -531,7 +617,6 @@ cudaError_t gemm_launch(const GemmPlan& plan, const uint8_t* W, int64_t n, int64
                         const void* X, int64_t m, int64_t ldx, void* Y, bool y_bf16,
                         int64_t ldy, void* workspace, int32_t* status, uint32_t flags,
                         cudaStream_t s) {
-  (void)workspace;
   const int64_t tiles = plan.n_tiles * plan.m_tiles;
   if (tiles > (int64_t(1) << 30)) return cudaErrorNotSupported;
   const int bn = plan.block_n;
@@ -567,9 +652,18 @@ cudaError_t gemm_launch(const GemmPlan& plan, const uint8_t* W, int64_t n, int64
   a.n_tiles = static_cast<int>(plan.n_tiles);
   a.tiles = static_cast<int>(tiles);
   a.x_stages = x_stages_for(bn);
+  a.splits = static_cast<int>(plan.splits);
+  a.counters = nullptr;
+  a.partials = nullptr;
+  if (plan.splits > 1) {
+    const size_t cnt = (static_cast<size_t>(tiles) * 4 + 255) / 256 * 256;
+    a.counters = static_cast<int32_t*>(workspace);
+    a.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + cnt);
+  }
   const int64_t g = sm_count();
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(tiles < g ? tiles : g));
+  const int64_t items = tiles * plan.splits;
+  cfg.gridDim = dim3(static_cast<unsigned>(items < g ? items : g));
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBudget;
   cfg.stream = s;

@@ -121,3 +121,20 @@ def test_linear_dispatch_matches_oracle(torch, q4, oracle_mod, m):
     Y, S = oracle_mod.matmul(W, n, k, xin)
     ok, info = within_tol(y, Y, S, 1e-4 if gemv_path else TOL)
     assert ok, info
+
+
+def test_gemm_split_k_leaves_workspace_zero(torch, q4, oracle_mod):
+    """Small M splits K across CTAs; the partial tiles live in the workspace and
+    must be cleared again, since GEMV calls share the same workspace."""
+    n, k, m = 4096, 3072, 8
+    W, _, _ = oracle_mod.quantize(synth.np_weights(n, k, seed=61))
+    x = synth.np_activations(m, k, seed=62)
+    ws = q4.Workspace()
+    xb = torch.from_numpy(x).to(torch.bfloat16).cuda()
+    y = q4.q4_gemm(torch.from_numpy(W).cuda(), n, k, xb, workspace=ws)
+    torch.cuda.synchronize()
+    assert q4.q4_gemm_workspace_bytes(n, k, m) > 0  # this shape does split K
+    assert int(ws.buf.count_nonzero().item()) == 0
+    Y, S = oracle_mod.matmul(W, n, k, xb.float().cpu().numpy())
+    ok, info = within_tol(y.cpu().numpy(), Y, S, 8e-3)
+    assert ok, info
