@@ -308,9 +308,10 @@ def _run_stack(args, world, dev, stream, hbm, peak_src, torch):
     achieved = (wbytes + abytes) / (ms_step * 1e-3) / 1e9
 
     # ---------------- e2e: host input -> step -> host output, every step
-    x_host = torch.empty((args.steps, 3072), dtype=torch.float32).pin_memory()
-    x_host.copy_(torch.randn((args.steps, 3072), generator=torch.Generator().manual_seed(7)))
-    y_host = torch.empty((args.steps, 3072), dtype=torch.float32).pin_memory()
+    rows = max(args.steps, 3)  # the 3 untimed warm-up steps use rows 0..2 too
+    x_host = torch.empty((rows, 3072), dtype=torch.float32).pin_memory()
+    x_host.copy_(torch.randn((rows, 3072), generator=torch.Generator().manual_seed(7)))
+    y_host = torch.empty((rows, 3072), dtype=torch.float32).pin_memory()
     x_dev = torch.empty((1, 3072), dtype=torch.float32, device=dev)
     g_e2e = dec.capture([x_dev], stream, chain=use_chain)
     with torch.cuda.stream(stream):

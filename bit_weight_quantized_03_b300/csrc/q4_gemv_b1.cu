@@ -15,9 +15,16 @@
 //     row).  Units are ordered row-group major; every warp takes one contiguous
 //     range of them ("stream-K"), so each warp gets the same number +-1.
 //   * Each warp streams its units through its own ring of shared-memory slots,
-//     one 2-D TMA tile (144 B x 32 rows, evict-first) per unit.  The ring is
-//     filled before waiting on the previous kernel (programmatic dependent
-//     launch), so weight reads overlap the previous layer's tail.
+//     one 2-D TMA tile (144 B x 32 rows, evict-first) per unit.
+//   * Two shapes of CTA.  Alone on the GPU, 16 warps per CTA and one CTA per
+//     SM; x is staged first and the ring filled behind it.  In a chain of
+//     dependent launches (programmatic dependent launch), 8 warps per CTA and
+//     at most ~113 KB of shared memory, so that the next product's CTA fits on
+//     the same SM beside the running one: it fills its ring (the weights do
+//     not depend on the previous product) and then waits, and when the
+//     previous product completes its first tiles are already on chip.  Above
+//     64 MB of weights the prefetch is too small a share and the solo shape
+//     is used even in a chain.
 //   * Lane l works on block pair j = l % 4 (weights 64j .. 64j+63 of the unit)
 //     of rows l/4, l/4 + 8, l/4 + 16, l/4 + 24.  Its 64 activations are loaded
 //     once per unit into registers as fp32 pairs and serve all four rows; the
@@ -30,9 +37,18 @@
 //     (q - 8) exactly for two weights, one packed fp32x2 FMA multiplies them by
 //     the adjacent activation pair.  Per block the 32 products are summed and
 //     scaled by d once.
-//   * Row groups split between warps are finished deterministically: partial
-//     row sums go to the workspace, the last warp to arrive (atomic counter)
-//     adds them in warp order, zeroes them and resets the counter.
+//   * Row groups split between warps are finished without atomics.  Each warp
+//     walks its range from the last unit down, so of the warps sharing a row
+//     group, the one that owns the group's last unit (its "reducer") reaches
+//     the group at the very end of its walk, and every other owner reaches it
+//     first.  Those store their 32 row sums as tagged 64-bit words (value and
+//     a presence tag in one single-copy-atomic store: no fence is needed, and
+//     the warp is free at once); the reducer, by then normally finding every
+//     word present, polls for any missing one (bounded wait), adds them in
+//     warp order (deterministic), clears them and writes y.  A warp publishes
+//     before it ever waits, and warps are numbered CTA by CTA, so a reducer
+//     waits only for its own CTA or CTAs placed before it; the wait is bounded
+//     all the same (Q4_ERR_TIMEOUT after about a second, never a hang).
 #include "q4_gemv_tile.cuh"
 
 namespace q4 {
@@ -42,29 +58,41 @@ using tile::unit_dot;
 using tile::xpad_floats;
 using tile::xpad_index;
 
-constexpr int kWarps = 16;                    // warps per CTA, one CTA per SM
 constexpr int kStages = 2;                    // ring slots per warp
 constexpr int kSlotBytes = 32 * kSuperBytes;  // 32 rows x 144 B
-constexpr int kRingBytes = kWarps * kStages * kSlotBytes;
-constexpr int kMaxSmem = 226 * 1024;  // dynamic part; the static barriers need the rest
+// Alone: 16 warps, one CTA per SM, up to 226 KB dynamic shared memory (the
+// static barriers take the rest of the 227 KB a CTA may hold).
+constexpr int kSoloWarps = 16;
+constexpr int kSoloMaxSmem = 226 * 1024;
+// In a chain: 8 warps, and two CTAs must fit in one SM's 228 KB (each CTA
+// also costs 1 KB of reserved shared memory and its static barriers).
+constexpr int kPairWarps = 8;
+constexpr int kPairMaxSmem = 115200;
+constexpr uint64_t kPairMaxWeightBytes = 64ull << 20;
+constexpr int ring_bytes(int warps) { return warps * kStages * kSlotBytes; }
 
 struct B1Params {
   const uint8_t* W;
   int64_t n, nsb;
   const float* x;
   float* y;
-  int32_t* counters;  // [groups]
-  float* partials;    // [warps][2][32]
+  int32_t* counters;   // [groups], unused here (left zero)
+  uint64_t* partials;  // [warps][32] tagged row sums, zero when empty
   int64_t units, warps;
   int32_t* status;
   uint32_t flags;
 };
 
-__device__ __forceinline__ int atomic_add_acq_rel_gpu(int32_t* p, int v) {
-  int old;
-  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
-               : "memory");
-  return old;
+// A partial row sum as one 64-bit word: the float's bits below a presence tag.
+constexpr uint64_t kPresent = 1ull << 32;
+
+__device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
 }
 
 // First unit of warp i when `units` units are cut into `warps` contiguous
@@ -76,15 +104,21 @@ __device__ __forceinline__ int64_t owner_of(int64_t u, int64_t units, int64_t wa
   return ((u + 1) * warps - 1) / units;
 }
 
-__global__ void __launch_bounds__(kWarps * 32, 1)
+// kWarps warps per CTA; kEarlyRing: fill the ring before waiting on the
+// previous kernel (the chain shape) rather than after staging x.
+template <int kWarps, bool kEarlyRing>
+__global__ void __launch_bounds__(kWarps * 32, 16 / kWarps)
     gemv_b1_kernel(const __grid_constant__ CUtensorMap tmap, const B1Params p) {
+  constexpr int kRingBytes = ring_bytes(kWarps);
+  static_assert(kRingBytes > 0, "ring");
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t bars[kWarps][kStages];
   __shared__ __align__(8) uint64_t never[kWarps];  // test hook: nothing ever arrives here
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // Warps are dealt to CTAs round-robin so that small matrices still spread
-  // over every SM.
-  const int64_t wid = static_cast<int64_t>(warp) * gridDim.x + blockIdx.x;
+  // Warps are numbered CTA by CTA, so a reducer (below) only ever waits for
+  // warps of its own CTA or of CTAs with a lower index, which were placed on
+  // the GPU before it.
+  const int64_t wid = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
   const bool active = wid < p.warps;
   const uint32_t xs = smem_u32(smem);
   const int64_t xpad = xpad_floats(p.nsb * kSuperElems);
@@ -95,7 +129,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
   const uint64_t pol = l2_evict_first_policy();
   const bool stall_test = (p.flags & kFlagTestStallOneWait) != 0 && wid == 0;
 
-  int64_t u0 = 0, nunits = 0, g_first = 0;
+  // The warp's range is [u0, u0 + nunits); it is walked from its last unit down.
+  int64_t u0 = 0, nunits = 0, g_top = 0, sb_top = 0;
   int64_t ig = 0, isb = 0, issued = 0;
   int islot = 0;
   if (active) {
@@ -107,11 +142,13 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     __syncwarp();
     u0 = range_start(wid, p.units, p.warps);
     nunits = range_start(wid + 1, p.units, p.warps) - u0;  // >= 1
-    g_first = u0 / p.nsb;
-    ig = g_first;
-    isb = u0 - g_first * p.nsb;
+    const int64_t u_last = u0 + nunits - 1;
+    g_top = u_last / p.nsb;
+    sb_top = u_last - g_top * p.nsb;
+    ig = g_top;
+    isb = sb_top;
   }
-  // Producer side: the next unit to load, walked without divisions.
+  // Producer side: the next unit to load, walked down without divisions.
   auto issue_next = [&]() {
     if (lane == 0) {
       const uint32_t bar = bar0 + 8 * islot;
@@ -120,13 +157,17 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
                        static_cast<int32_t>(ig * 32), bar, pol);
     }
     ++issued;
-    if (++isb == p.nsb) {
-      isb = 0;
-      ++ig;
+    if (isb-- == 0) {
+      isb = p.nsb - 1;
+      --ig;
     }
     if (++islot == kStages) islot = 0;
   };
   pdl_allow_dependents();
+  // The weights never depend on the previous kernel: in the chain shape the
+  // ring is filled while that kernel still runs.
+  if (kEarlyRing)
+    while (issued < nunits && issued < kStages) issue_next();
   pdl_wait_prior_grid();  // x, y and the workspace are now safe to touch
 
   // Stage x (all of it) into shared memory with the padded layout.  Its loads
@@ -142,7 +183,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
       const int i = static_cast<int>(threadIdx.x) + t * kWarps * 32;
       if (i < k4) xv[t] = __ldg(xg + i);
     }
-    while (issued < nunits && issued < kStages) issue_next();
+    if (!kEarlyRing)
+      while (issued < nunits && issued < kStages) issue_next();
     auto put = [&](int i, const float4& v) {
       asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(xs + 4 * xpad_index(4 * i)),
                    "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
@@ -164,8 +206,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
   const int rr = lane >> 2;  // rows rr, rr + 8, rr + 16, rr + 24 of the group
   float yv[4] = {0.f, 0.f, 0.f, 0.f};
 
-  // Consumer side: unit `done` of the range is (g, sb) in ring slot `slot`.
-  int64_t g = g_first, sb = u0 - g_first * p.nsb, done = 0;
+  // Consumer side: unit `done` of the walk is (g, sb) in ring slot `slot`.
+  int64_t g = g_top, sb = sb_top, done = 0;
   int slot = 0;
   uint32_t parity = 0;
   bool ok = true;
@@ -183,7 +225,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     __syncwarp();
     fence_proxy_async_smem();
     if (issued < nunits) issue_next();
-    if (sb == p.nsb - 1 || done == nunits - 1) {
+    if (sb == 0 || done == nunits - 1) {
       // Row group g is done for this warp: the four lanes of a quad hold the
       // four block-pair sums of the same rows; add them (fixed order).
       float v[4];
@@ -204,54 +246,65 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
           }
         }
       } else {
-        // Partial slot 0 holds a warp's first row group, slot 1 its last.
-        float* mine = p.partials + (wid * 2 + (g == g_first ? 0 : 1)) * 32;
-        if (j == 0) {
+        // Lane l takes row l's sum: rows rr + 8i sit in quad rr (lane 4rr).
+        float mine = 0.f;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) __stcg(mine + rr + 8 * i, v[i]);
+        for (int i = 0; i < 4; ++i) {
+          const float t = __shfl_sync(0xffffffffu, v[i], 4 * (lane & 7));
+          if ((lane >> 3) == i) mine = t;
         }
-        __syncwarp();  // the lanes' partials are ordered before lane 0's release
-        const int64_t i0 = owner_of(gu0, p.units, p.warps);
-        const int64_t i1 = owner_of(gu1 - 1, p.units, p.warps);
-        int last = 0;
-        // acq_rel: releases this warp's partials; the last arrival acquires all
-        if (lane == 0) last = atomic_add_acq_rel_gpu(&p.counters[g], 1) == static_cast<int>(i1 - i0);
-        last = __shfl_sync(0xffffffffu, last, 0);
-        if (last) {
-          // Owner i0 may have started in an earlier group (then this group is
-          // its slot 1); every later owner starts inside this group (slot 0).
-          const int64_t i0_slot = range_start(i0, p.units, p.warps) < gu0 ? 1 : 0;
-          const int np = static_cast<int>(i1 - i0 + 1);
+        if (u0 + nunits < gu1) {
+          // not the reducer: publish and move on
+          st_relaxed_u64(p.partials + wid * 32 + lane, kPresent | __float_as_uint(mine));
+        } else {
+          // reducer (owns unit gu1 - 1): owners i0 .. wid - 1 published theirs
+          const int64_t i0 = owner_of(gu0, p.units, p.warps);
           float s = 0.f;
-          for (int b = 0; b < np; b += 8) {
-            float pv[8];
+          const uint64_t t0 = global_timer_ns();
+          for (int64_t b = i0; b < wid; b += 8) {
+            // Poll a batch of up to 8 owners: every pass re-reads all the words
+            // still missing at once, so late owners cost one round trip together.
+            uint64_t pv[8];
 #pragma unroll
-            for (int t = 0; t < 8; ++t) {
-              const int64_t i = i0 + b + t;
-              const int64_t sl = (t == 0 && b == 0) ? i0_slot : 0;
-              pv[t] = (b + t < np) ? __ldcg(p.partials + (i * 2 + sl) * 32 + lane) : 0.f;
+            for (int t = 0; t < 8; ++t) pv[t] = 0;
+            while (true) {
+#pragma unroll
+              for (int t = 0; t < 8; ++t)
+                if (b + t < wid && !(pv[t] & kPresent))
+                  pv[t] = ld_relaxed_u64(p.partials + (b + t) * 32 + lane);
+              bool all = true;
+#pragma unroll
+              for (int t = 0; t < 8; ++t) all = all && (b + t >= wid || (pv[t] & kPresent));
+              if (all) break;
+              if (global_timer_ns() - t0 > kWaitLimitNs) {
+                ok = false;
+                break;
+              }
             }
 #pragma unroll
-            for (int t = 0; t < 8; ++t)
-              if (b + t < np) s += pv[t];  // warp order: deterministic
+            for (int t = 0; t < 8; ++t)  // warp order: deterministic
+              if (b + t < wid) s += __uint_as_float(static_cast<uint32_t>(pv[t]));
           }
-          for (int b = 0; b < np; ++b) {  // the workspace goes back to all-zero
-            const int64_t sl = b == 0 ? i0_slot : 0;
-            __stcg(p.partials + ((i0 + b) * 2 + sl) * 32 + lane, 0.f);
-          }
+          s += mine;
+          for (int64_t b = i0; b < wid; ++b)  // the workspace goes back to all-zero
+            st_relaxed_u64(p.partials + b * 32 + lane, 0ull);
           const int64_t row = g * 32 + lane;
           if (row < p.n) p.y[row] = s;
-          if (lane == 0) p.counters[g] = 0;
+          if (!__all_sync(0xffffffffu, ok)) ok = false;
         }
       }
     }
-    if (++sb == p.nsb) {
-      sb = 0;
-      ++g;
+    if (sb-- == 0) {
+      sb = p.nsb - 1;
+      --g;
     }
     if (++slot == kStages) {
       slot = 0;
       parity ^= 1u;
+    }
+    if (!ok) {
+      ++done;  // this unit's copy has been consumed
+      break;
     }
   }
 
@@ -265,17 +318,52 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
   }
 }
 
+size_t b1_smem_bytes(int64_t k, int warps) {
+  return static_cast<size_t>((xpad_floats(k) * 4 + 127) / 128 * 128 + ring_bytes(warps));
+}
+
+template <int W, bool E>
+cudaError_t launch_shape(const CUtensorMap& tmap, const B1Params& p, size_t smem, int max_smem,
+                         bool pdl, cudaStream_t s) {
+  static bool configured[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(gemv_b1_kernel<W, E>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+    if (e != cudaSuccess) return e;
+    // All of the SM's unified L1/shared storage as shared memory, so that a
+    // second CTA can be placed beside a running one without a reconfiguration.
+    e = cudaFuncSetAttribute(gemv_b1_kernel<W, E>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             100);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  const int64_t sms = sm_count();
+  const int64_t ctas = (p.warps + W - 1) / W;  // <= sms: warps <= sms * W
+  cfg.gridDim = dim3(static_cast<unsigned>(ctas < sms ? ctas : sms));
+  cfg.blockDim = dim3(W * 32);
+  cfg.dynamicSmemBytes = static_cast<unsigned>(smem);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, gemv_b1_kernel<W, E>, tmap, p);
+}
+
 }  // namespace
 
+// Warps of the solo shape; the chain shape uses no more (the workspace is
+// sized from this count).
 int64_t gemv_b1_warps(int64_t units) {
-  const int64_t target = static_cast<int64_t>(sm_count()) * kWarps;
+  const int64_t target = static_cast<int64_t>(sm_count()) * kSoloWarps;
   return units < target ? units : target;
 }
 
-bool gemv_b1_supports(int64_t k) {
-  const int64_t xbytes = (xpad_floats(k) * 4 + 127) / 128 * 128;
-  return xbytes + kRingBytes <= kMaxSmem;
-}
+bool gemv_b1_supports(int64_t k) { return b1_smem_bytes(k, kSoloWarps) <= kSoloMaxSmem; }
 
 cudaError_t gemv_b1_launch(const uint8_t* W, int64_t n, int64_t k, const float* x, float* y,
                            int32_t* counters, float* partials, int64_t units, int64_t warps,
@@ -286,15 +374,7 @@ cudaError_t gemv_b1_launch(const uint8_t* W, int64_t n, int64_t k, const float* 
                       static_cast<uint64_t>(n), static_cast<uint64_t>(rowbytes), kSuperBytes, 32,
                       CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
-  static bool configured[64] = {false};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(gemv_b1_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
-    if (e != cudaSuccess) return e;
-    configured[dev] = true;
-  }
+  const bool pdl = (flags & 1u) != 0;
   B1Params p;
   p.W = W;
   p.n = n;
@@ -302,24 +382,24 @@ cudaError_t gemv_b1_launch(const uint8_t* W, int64_t n, int64_t k, const float* 
   p.x = x;
   p.y = y;
   p.counters = counters;
-  p.partials = partials;
+  p.partials = reinterpret_cast<uint64_t*>(partials);
   p.units = units;
-  p.warps = warps;
   p.status = status;
   p.flags = flags;
-  cudaLaunchConfig_t cfg = {};
-  const int64_t sms = sm_count();
-  cfg.gridDim = dim3(static_cast<unsigned>(warps < sms ? warps : sms));
-  cfg.blockDim = dim3(kWarps * 32);
-  cfg.dynamicSmemBytes =
-      static_cast<unsigned>((xpad_floats(k) * 4 + 127) / 128 * 128 + kRingBytes);
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = (flags & 1u) ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, gemv_b1_kernel, tmap, p);
+  const size_t pair_smem = b1_smem_bytes(k, kPairWarps);
+  // The chain shape pays while the next product's ring fill is a real share of
+  // that product: for the 7-32 MB decoder products it takes ~13 % off a decode
+  // step, for the 226 MB output head the solo shape is faster (53 vs 56 us).
+  const bool pair_worth =
+      static_cast<uint64_t>(n) * static_cast<uint64_t>(rowbytes) <= kPairMaxWeightBytes;
+  if (pdl && pair_worth && pair_smem <= static_cast<size_t>(kPairMaxSmem)) {
+    const int64_t target = static_cast<int64_t>(sm_count()) * kPairWarps;
+    p.warps = units < target ? units : target;  // <= warps: the workspace holds its partials
+    return launch_shape<kPairWarps, true>(tmap, p, pair_smem, kPairMaxSmem, pdl, s);
+  }
+  p.warps = warps;
+  return launch_shape<kSoloWarps, false>(tmap, p, b1_smem_bytes(k, kSoloWarps), kSoloMaxSmem,
+                                          pdl, s);
 }
 
 }  // namespace q4

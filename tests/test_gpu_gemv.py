@@ -53,6 +53,27 @@ def test_gemv_matches_oracle(torch, q4, oracle_mod, n, k, m):
     assert ok, info
 
 
+# Batch-1 calls with the PDL flag take the chain shape of the batch-1 kernel
+# (8 warps per CTA, ring filled before the wait on the previous kernel) while
+# its shared memory lets two CTAs share an SM (k up to 9216 here); k = 10240
+# does not fit and falls back to the solo shape.
+PDL_SHAPES = [(1, 256, 1), (4095, 256, 1), (4096, 3072, 1), (6144, 3072, 1), (257, 9216, 1),
+              (3072, 9216, 1), (100, 10240, 1)]
+
+
+@pytest.mark.parametrize("n,k,m", PDL_SHAPES)
+def test_gemv_pdl_shape_matches_oracle(torch, q4, oracle_mod, n, k, m):
+    W, x = _case(oracle_mod, n, k, m, seed=3 * n + k)
+    Y, S = oracle_mod.matmul(W, n, k, x, nthreads=oracle_mod.cpu_count())
+    ws = q4.Workspace()
+    ys = [_gemv(torch, q4, W, n, k, x, flags=q4.FLAG_PDL, workspace=ws) for _ in range(2)]
+    ok, info = within_tol(ys[0], Y, S, TOL)
+    assert ok, info
+    assert np.array_equal(ys[1].view(np.uint32), ys[0].view(np.uint32))  # deterministic
+    torch.cuda.synchronize()
+    assert int(ws.buf.count_nonzero().item()) == 0
+
+
 def test_gemv_strided_x_and_y(torch, q4, oracle_mod):
     n, k, m = 300, 1024, 3
     W, x = _case(oracle_mod, n, k, m, seed=5)
@@ -119,15 +140,18 @@ def test_gemv_workspace_left_zeroed(torch, q4, oracle_mod):
     assert int(ws.buf[:cnt_bytes].count_nonzero().item()) == 0
 
 
-def test_gemv_bounded_wait_reports_timeout(torch, q4, oracle_mod):
+@pytest.mark.parametrize("pdl", [False, True])
+def test_gemv_bounded_wait_reports_timeout(torch, q4, oracle_mod, pdl):
     """A wait that nothing completes (test flag) ends with Q4_ERR_TIMEOUT in the
-    status word after about a second; the context stays usable."""
+    status word after about a second; the context stays usable.  With the PDL
+    flag the batch-1 kernel runs in its chain shape."""
     n, k = 64, 512
     W, x = _case(oracle_mod, n, k, 1, seed=40)
     ws = q4.Workspace()
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    flags = q4.FLAG_TEST_STALL | (q4.FLAG_PDL if pdl else 0)
     q4.q4_gemv(torch.from_numpy(W).cuda(), n, k, torch.from_numpy(x).cuda(), workspace=ws,
-               status=st, flags=q4.FLAG_TEST_STALL)
+               status=st, flags=flags)
     torch.cuda.synchronize()
     assert int(st.item()) == q4.ERR_TIMEOUT
     ws.reset()
