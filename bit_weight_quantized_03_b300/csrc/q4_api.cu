@@ -234,12 +234,14 @@ q4_status q4_gemv_chain(const q4_gemv_stage* stages, int32_t n_stages, void* wor
 int64_t q4_linear_crossover_m(int64_t n, int64_t k) {
   (void)n;
   // Largest batch still sent to the fp32 GEMV.  Measured on B300 on the
-  // 4096 x 3072 decoder shape (L2-cold, CUDA graphs): the batch-1 GEMV takes
-  // 6.5 us; from two streams on, the split-K tensor-core GEMM (13.6 us at
-  // M = 2, 17 us at M = 16) beats the multi-row GEMV (15.5 us at M = 2).  The
-  // tensor-core path needs k % 256 == 0.
+  // 4096 x 3072 decoder shape (L2-cold, CUDA graphs): the GEMV takes 5.1 /
+  // 7.2 / 9.9 us for 1 / 2 / 4 rows of x (one launch of the batched tile
+  // kernel up to 4 rows), the split-K tensor-core GEMM 13.5-13.7 us for
+  // M = 1..4 and 14.8 us at M = 8, where the GEMV needs two launches (19.4 us);
+  // at M = 5..7 a 4-row launch plus the rest already costs more than the GEMM.
+  // The tensor-core path needs k % 256 == 0.
   if (k % 256 != 0) return Q4_GEMV_MAX_M;
-  return 1;
+  return 4;
 }
 
 size_t q4_linear_workspace_bytes(int64_t n, int64_t k, int64_t m, q4_dtype x_dtype) {

@@ -8,6 +8,12 @@
 // used once, so the product is bound by HBM bandwidth; the design keeps the
 // weight stream in flight and the per-weight instruction count low.
 //
+// Dispatch (gemv_launch): k % 256 == 0 goes to the tile kernels of
+// q4_gemv_b1.cu -- one row of x to the batch-1 kernel, 2..16 rows to launches of
+// up to 4 rows of the batched tile kernel (each unit decoded once for all of
+// its rows).  The streamed kernel below serves the rows those cannot take (x
+// too wide for shared memory); the generic kernel any k % 32 == 0.
+//
 // Streamed kernel (k % 256 == 0):
 //   * Work unit = 32 rows x 256 weights (8 blocks = 144 contiguous, 16-byte
 //     aligned bytes per row).  Units are ordered row-group major and every warp
@@ -18,9 +24,9 @@
 //     matrix, evict-first L2 hint), completion counted on the slot's mbarrier.
 //     (Thirty-two 144-byte bulk copies per unit instead were bound by the copy
 //     engine's per-request cost.)  Slot rows are 144 B apart (9 x 16 B, odd), so
-//     each lane's 16-byte shared loads of its row are bank-conflict free.  The ring is filled before waiting on the previous
-//     kernel (programmatic dependent launch), so weight reads overlap the
-//     previous layer's tail.
+//     each lane's 16-byte shared loads of its row are bank-conflict free.  The
+//     ring is filled before waiting on the previous kernel (programmatic
+//     dependent launch), so weight reads overlap the previous layer's tail.
 //   * Decode: a nibble sitting at bit p <= 16 of a 32-bit word becomes the float
 //     2^(23-p) + q with one AND/OR (LOP3); one packed subtract gives (q - 8)
 //     exactly for two weights.  Weights are paired with the adjacent activation
@@ -428,10 +434,18 @@ GemvPlan gemv_plan(int64_t n, int64_t k, int64_t m) {
   if (!p.fast) return p;
   p.units = p.groups * (k / kSuperElems);
   p.b1 = (m == 1) && gemv_b1_supports(k);
+  // 2..16 rows: launches of up to kMaxBatchRows rows of the batched tile
+  // kernel (a single leftover row goes to the batch-1 kernel)
+  p.bm = (m >= 2) && gemv_bm_supports(k, 2) && gemv_b1_supports(k);
   const int64_t target = static_cast<int64_t>(sm_count()) * kCtasPerSm * kWarps;
   p.warps = p.b1 ? gemv_b1_warps(p.units) : (p.units < target ? p.units : target);
   const size_t cnt_bytes = (static_cast<size_t>(p.groups) * 4 + 255) / 256 * 256;
-  p.ws_bytes = cnt_bytes + static_cast<size_t>(p.warps) * 2 * static_cast<size_t>(m) * 32 * 4;
+  size_t part = static_cast<size_t>(p.warps) * 2 * static_cast<size_t>(m) * 32 * 4;
+  if (p.bm) {  // [warps][rows of the launch][32] tagged words of 8 bytes
+    part = std::max(part, static_cast<size_t>(gemv_bm_warps(p.units)) * kMaxBatchRows * 32 * 8);
+    part = std::max(part, static_cast<size_t>(gemv_b1_warps(p.units)) * 32 * 8);
+  }
+  p.ws_bytes = cnt_bytes + part;
   return p;
 }
 
@@ -444,6 +458,31 @@ cudaError_t gemv_launch(const GemvPlan& plan, const uint8_t* W, int64_t n, int64
     return gemv_b1_launch(W, n, k, x, y, static_cast<int32_t*>(workspace),
                           reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + cnt_bytes),
                           plan.units, plan.warps, status, flags, s);
+  }
+  if (plan.fast && plan.bm && m >= 2) {
+    // Launches of up to kMaxBatchRows rows (fewer where x would not fit in
+    // shared memory), in order on the stream; each leaves the workspace zero
+    // for the next, and under PDL a launch touches it only after the wait.
+    const size_t cnt_bytes = (static_cast<size_t>(plan.groups) * 4 + 255) / 256 * 256;
+    int32_t* counters = static_cast<int32_t*>(workspace);
+    float* partials = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + cnt_bytes);
+    for (int64_t r0 = 0; r0 < m;) {
+      const int64_t rem = m - r0;
+      cudaError_t e;
+      int64_t c = 1;
+      if (rem == 1) {
+        e = gemv_b1_launch(W, n, k, x + r0 * ldx, y + r0 * ldy, counters, partials, plan.units,
+                           gemv_b1_warps(plan.units), status, flags, s);
+      } else {
+        c = std::min(rem, kMaxBatchRows);
+        while (c > 2 && !gemv_bm_supports(k, c)) --c;
+        e = gemv_bm_launch(W, n, k, x + r0 * ldx, c, ldx, y + r0 * ldy, ldy, counters, partials,
+                           plan.units, status, flags, s);
+      }
+      if (e != cudaSuccess) return e;
+      r0 += c;
+    }
+    return cudaSuccess;
   }
   switch (m) {
 #define Q4_GEMV_CASE(MM) \

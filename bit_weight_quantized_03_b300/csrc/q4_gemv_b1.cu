@@ -55,6 +55,7 @@ namespace q4 {
 namespace {
 
 using tile::unit_dot;
+using tile::unit_dot_m;
 using tile::xpad_floats;
 using tile::xpad_index;
 
@@ -74,10 +75,11 @@ constexpr int ring_bytes(int warps) { return warps * kStages * kSlotBytes; }
 struct B1Params {
   const uint8_t* W;
   int64_t n, nsb;
-  const float* x;
-  float* y;
+  const float* x;      // [MB][ldx] (MB = rows of x per launch, 1..4)
+  float* y;            // [MB][ldy]
+  int64_t ldx, ldy;
   int32_t* counters;   // [groups], unused here (left zero)
-  uint64_t* partials;  // [warps][32] tagged row sums, zero when empty
+  uint64_t* partials;  // [warps][MB][32] tagged row sums, zero when empty
   int64_t units, warps;
   int32_t* status;
   uint32_t flags;
@@ -104,13 +106,15 @@ __device__ __forceinline__ int64_t owner_of(int64_t u, int64_t units, int64_t wa
   return ((u + 1) * warps - 1) / units;
 }
 
+constexpr int64_t xrow_bytes(int64_t k) { return (xpad_floats(k) * 4 + 127) / 128 * 128; }
+
 // kWarps warps per CTA; kEarlyRing: fill the ring before waiting on the
-// previous kernel (the chain shape) rather than after staging x.
-template <int kWarps, bool kEarlyRing>
-__global__ void __launch_bounds__(kWarps * 32, 16 / kWarps)
-    gemv_b1_kernel(const __grid_constant__ CUtensorMap tmap, const B1Params p) {
+// previous kernel (the chain shape) rather than after staging x; MB rows of x
+// (each unit is decoded once and applied to all of them).
+template <int kWarps, bool kEarlyRing, int MB>
+__device__ __forceinline__ void gemv_tile_body(const CUtensorMap& tmap, const B1Params& p) {
   constexpr int kRingBytes = ring_bytes(kWarps);
-  static_assert(kRingBytes > 0, "ring");
+  static_assert(kRingBytes > 0 && MB >= 1 && MB <= 4, "shape");
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t bars[kWarps][kStages];
   __shared__ __align__(8) uint64_t never[kWarps];  // test hook: nothing ever arrives here
@@ -121,8 +125,8 @@ __global__ void __launch_bounds__(kWarps * 32, 16 / kWarps)
   const int64_t wid = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
   const bool active = wid < p.warps;
   const uint32_t xs = smem_u32(smem);
-  const int64_t xpad = xpad_floats(p.nsb * kSuperElems);
-  const uint32_t ring = xs + static_cast<uint32_t>((xpad * 4 + 127) / 128 * 128);
+  const uint32_t xrow = static_cast<uint32_t>(xrow_bytes(p.nsb * kSuperElems));
+  const uint32_t ring = xs + MB * xrow;
   const uint32_t slots = ring + warp * (kStages * kSlotBytes);
   const uint32_t bar0 = smem_u32(&bars[warp][0]);
   const uint32_t never_bar = smem_u32(&never[warp]);
@@ -173,7 +177,7 @@ __global__ void __launch_bounds__(kWarps * 32, 16 / kWarps)
   // Stage x (all of it) into shared memory with the padded layout.  Its loads
   // are issued before the weight stream starts, so that they are not queued
   // behind the first units' tile loads.
-  {
+  if constexpr (MB == 1) {
     constexpr int kXRegs = 5;  // covers k <= 5 * 4 * 512 = 10240 in one pass
     const int k4 = static_cast<int>(p.nsb * (kSuperElems / 4));
     const float4* xg = reinterpret_cast<const float4*>(p.x);
@@ -197,6 +201,18 @@ __global__ void __launch_bounds__(kWarps * 32, 16 / kWarps)
     }
     for (int i = static_cast<int>(threadIdx.x) + kXRegs * kWarps * 32; i < k4; i += kWarps * 32)
       put(i, __ldg(xg + i));
+  } else {
+    const int k4 = static_cast<int>(p.nsb * (kSuperElems / 4));
+    if (!kEarlyRing)
+      while (issued < nunits && issued < kStages) issue_next();
+    for (int i = static_cast<int>(threadIdx.x); i < MB * k4; i += kWarps * 32) {
+      const int m = i / k4, c = i - m * k4;
+      const float4 v = __ldg(reinterpret_cast<const float4*>(p.x + m * p.ldx) + c);
+      asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(xs + m * xrow +
+                                                                     4 * xpad_index(4 * c)),
+                   "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
+                   : "memory");
+    }
   }
   __syncthreads();
   if (!active) return;
@@ -204,7 +220,11 @@ __global__ void __launch_bounds__(kWarps * 32, 16 / kWarps)
   const DecodeConsts dc = make_consts();
   const int j = lane & 3;    // block pair within the unit
   const int rr = lane >> 2;  // rows rr, rr + 8, rr + 16, rr + 24 of the group
-  float yv[4] = {0.f, 0.f, 0.f, 0.f};
+  float yv[MB][4];
+#pragma unroll
+  for (int m = 0; m < MB; ++m)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) yv[m][i] = 0.f;
 
   // Consumer side: unit `done` of the walk is (g, sb) in ring slot `slot`.
   int64_t g = g_top, sb = sb_top, done = 0;
@@ -221,48 +241,67 @@ __global__ void __launch_bounds__(kWarps * 32, 16 / kWarps)
       ok = false;
       break;
     }
-    unit_dot(slots + slot * kSlotBytes, xs, static_cast<int>(sb), j, rr, dc, yv);
+    if constexpr (MB == 1)
+      unit_dot(slots + slot * kSlotBytes, xs, static_cast<int>(sb), j, rr, dc, yv[0]);
+    else
+      unit_dot_m<MB>(slots + slot * kSlotBytes, xs, xrow, static_cast<int>(sb), j, rr, dc, yv);
     __syncwarp();
     fence_proxy_async_smem();
     if (issued < nunits) issue_next();
     if (sb == 0 || done == nunits - 1) {
       // Row group g is done for this warp: the four lanes of a quad hold the
       // four block-pair sums of the same rows; add them (fixed order).
-      float v[4];
+      float v[MB][4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        v[i] = yv[i];
-        v[i] += __shfl_xor_sync(0xffffffffu, v[i], 1);
-        v[i] += __shfl_xor_sync(0xffffffffu, v[i], 2);
-        yv[i] = 0.f;
-      }
+      for (int m = 0; m < MB; ++m)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          v[m][i] = yv[m][i];
+          v[m][i] += __shfl_xor_sync(0xffffffffu, v[m][i], 1);
+          v[m][i] += __shfl_xor_sync(0xffffffffu, v[m][i], 2);
+          yv[m][i] = 0.f;
+        }
       const int64_t gu0 = g * p.nsb, gu1 = gu0 + p.nsb;
       if (gu0 >= u0 && gu1 <= u0 + nunits) {
         if (j == 0) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int64_t row = g * 32 + rr + 8 * i;
-            if (row < p.n) p.y[row] = v[i];
-          }
+          for (int m = 0; m < MB; ++m)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int64_t row = g * 32 + rr + 8 * i;
+              if (row < p.n) p.y[m * p.ldy + row] = v[m][i];
+            }
         }
       } else {
-        // Lane l takes row l's sum: rows rr + 8i sit in quad rr (lane 4rr).
-        float mine = 0.f;
+        // Lane l takes row l's sums: rows rr + 8i sit in quad rr (lane 4rr).
+        float mine[MB];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float t = __shfl_sync(0xffffffffu, v[i], 4 * (lane & 7));
-          if ((lane >> 3) == i) mine = t;
+        for (int m = 0; m < MB; ++m) {
+          mine[m] = 0.f;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float t = __shfl_sync(0xffffffffu, v[m][i], 4 * (lane & 7));
+            if ((lane >> 3) == i) mine[m] = t;
+          }
         }
         if (u0 + nunits < gu1) {
           // not the reducer: publish and move on
-          st_relaxed_u64(p.partials + wid * 32 + lane, kPresent | __float_as_uint(mine));
+#pragma unroll
+          for (int m = 0; m < MB; ++m)
+            st_relaxed_u64(p.partials + (wid * MB + m) * 32 + lane,
+                           kPresent | __float_as_uint(mine[m]));
         } else {
-          // reducer (owns unit gu1 - 1): owners i0 .. wid - 1 published theirs
+          // reducer (owns unit gu1 - 1): owners i0 .. wid - 1 published MB
+          // words each, owner-major, so they form one run of `items` words.
           const int64_t i0 = owner_of(gu0, p.units, p.warps);
-          float s = 0.f;
+          const int64_t items = (wid - i0) * MB;
+          uint64_t* const run = p.partials + i0 * MB * 32 + lane;
+          float s[MB];
+#pragma unroll
+          for (int m = 0; m < MB; ++m) s[m] = 0.f;
           const uint64_t t0 = global_timer_ns();
-          for (int64_t b = i0; b < wid; b += 8) {
-            // Poll a batch of up to 8 owners: every pass re-reads all the words
+          for (int64_t b = 0; b < items; b += 8) {
+            // Poll a batch of up to 8 words: every pass re-reads all the words
             // still missing at once, so late owners cost one round trip together.
             uint64_t pv[8];
 #pragma unroll
@@ -270,26 +309,35 @@ __global__ void __launch_bounds__(kWarps * 32, 16 / kWarps)
             while (true) {
 #pragma unroll
               for (int t = 0; t < 8; ++t)
-                if (b + t < wid && !(pv[t] & kPresent))
-                  pv[t] = ld_relaxed_u64(p.partials + (b + t) * 32 + lane);
+                if (b + t < items && !(pv[t] & kPresent)) pv[t] = ld_relaxed_u64(run + (b + t) * 32);
               bool all = true;
 #pragma unroll
-              for (int t = 0; t < 8; ++t) all = all && (b + t >= wid || (pv[t] & kPresent));
+              for (int t = 0; t < 8; ++t) all = all && (b + t >= items || (pv[t] & kPresent));
               if (all) break;
               if (global_timer_ns() - t0 > kWaitLimitNs) {
                 ok = false;
                 break;
               }
             }
+            const int m0 = static_cast<int>(b % MB);
 #pragma unroll
-            for (int t = 0; t < 8; ++t)  // warp order: deterministic
-              if (b + t < wid) s += __uint_as_float(static_cast<uint32_t>(pv[t]));
+            for (int t = 0; t < 8; ++t) {  // owner order within each row of x: deterministic
+              if (b + t >= items) continue;
+              const float val = __uint_as_float(static_cast<uint32_t>(pv[t]));
+              const int mt = (m0 + t) % MB;
+#pragma unroll
+              for (int m = 0; m < MB; ++m)
+                if (mt == m) s[m] += val;
+            }
           }
-          s += mine;
-          for (int64_t b = i0; b < wid; ++b)  // the workspace goes back to all-zero
-            st_relaxed_u64(p.partials + b * 32 + lane, 0ull);
+          for (int64_t b = 0; b < items; ++b)  // the workspace goes back to all-zero
+            st_relaxed_u64(run + b * 32, 0ull);
           const int64_t row = g * 32 + lane;
-          if (row < p.n) p.y[row] = s;
+#pragma unroll
+          for (int m = 0; m < MB; ++m) {
+            s[m] += mine[m];
+            if (row < p.n) p.y[m * p.ldy + row] = s[m];
+          }
           if (!__all_sync(0xffffffffu, ok)) ok = false;
         }
       }
@@ -318,24 +366,37 @@ __global__ void __launch_bounds__(kWarps * 32, 16 / kWarps)
   }
 }
 
-size_t b1_smem_bytes(int64_t k, int warps) {
-  return static_cast<size_t>((xpad_floats(k) * 4 + 127) / 128 * 128 + ring_bytes(warps));
+template <int kWarps, bool kEarlyRing>
+__global__ void __launch_bounds__(kWarps * 32, 16 / kWarps)
+    gemv_b1_kernel(const __grid_constant__ CUtensorMap tmap, const B1Params p) {
+  gemv_tile_body<kWarps, kEarlyRing, 1>(tmap, p);
 }
 
-template <int W, bool E>
-cudaError_t launch_shape(const CUtensorMap& tmap, const B1Params& p, size_t smem, int max_smem,
-                         bool pdl, cudaStream_t s) {
-  static bool configured[64] = {false};
+// 2..4 rows of x (batched decode): 8 warps, registers uncapped.
+template <int MB, bool kEarlyRing>
+__global__ void __launch_bounds__(kPairWarps * 32, 1)
+    gemv_bm_kernel(const __grid_constant__ CUtensorMap tmap, const B1Params p) {
+  gemv_tile_body<kPairWarps, kEarlyRing, MB>(tmap, p);
+}
+
+size_t b1_smem_bytes(int64_t k, int warps, int mb = 1) {
+  return static_cast<size_t>(mb * xrow_bytes(k) + ring_bytes(warps));
+}
+
+// Launches one of the kernels above (W warps per CTA) once its attributes are
+// set on the current device.
+template <int W, typename Kernel>
+cudaError_t launch_tiles(Kernel kernel, bool (&configured)[64], const CUtensorMap& tmap,
+                         const B1Params& p, size_t smem, int max_smem, bool pdl, cudaStream_t s) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(gemv_b1_kernel<W, E>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+    cudaError_t e =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
     if (e != cudaSuccess) return e;
     // All of the SM's unified L1/shared storage as shared memory, so that a
     // second CTA can be placed beside a running one without a reconfiguration.
-    e = cudaFuncSetAttribute(gemv_b1_kernel<W, E>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             100);
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
@@ -351,7 +412,29 @@ cudaError_t launch_shape(const CUtensorMap& tmap, const B1Params& p, size_t smem
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, gemv_b1_kernel<W, E>, tmap, p);
+  return cudaLaunchKernelEx(&cfg, kernel, tmap, p);
+}
+
+template <int W, bool E>
+cudaError_t launch_shape(const CUtensorMap& tmap, const B1Params& p, size_t smem, int max_smem,
+                         bool pdl, cudaStream_t s) {
+  static bool configured[64] = {false};
+  return launch_tiles<W>(gemv_b1_kernel<W, E>, configured, tmap, p, smem, max_smem, pdl, s);
+}
+
+template <int MB, bool E>
+cudaError_t launch_batched(const CUtensorMap& tmap, const B1Params& p, size_t smem, bool pdl,
+                           cudaStream_t s) {
+  static bool configured[64] = {false};
+  return launch_tiles<kPairWarps>(gemv_bm_kernel<MB, E>, configured, tmap, p, smem,
+                                  kSoloMaxSmem, pdl, s);
+}
+
+bool make_tmap(CUtensorMap* tmap, const uint8_t* W, int64_t n, int64_t k) {
+  const int64_t rowbytes = k / 32 * kBlockBytes;
+  return encode_tmap_2d(tmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, static_cast<uint64_t>(rowbytes),
+                        static_cast<uint64_t>(n), static_cast<uint64_t>(rowbytes), kSuperBytes,
+                        32, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 }  // namespace
@@ -370,10 +453,7 @@ cudaError_t gemv_b1_launch(const uint8_t* W, int64_t n, int64_t k, const float* 
                            int32_t* status, uint32_t flags, cudaStream_t s) {
   const int64_t rowbytes = k / 32 * kBlockBytes;
   CUtensorMap tmap;
-  if (!encode_tmap_2d(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, static_cast<uint64_t>(rowbytes),
-                      static_cast<uint64_t>(n), static_cast<uint64_t>(rowbytes), kSuperBytes, 32,
-                      CU_TENSOR_MAP_SWIZZLE_NONE))
-    return cudaErrorInvalidValue;
+  if (!make_tmap(&tmap, W, n, k)) return cudaErrorInvalidValue;
   const bool pdl = (flags & 1u) != 0;
   B1Params p;
   p.W = W;
@@ -381,6 +461,8 @@ cudaError_t gemv_b1_launch(const uint8_t* W, int64_t n, int64_t k, const float* 
   p.nsb = k / kSuperElems;
   p.x = x;
   p.y = y;
+  p.ldx = k;
+  p.ldy = n;
   p.counters = counters;
   p.partials = reinterpret_cast<uint64_t*>(partials);
   p.units = units;
@@ -400,6 +482,49 @@ cudaError_t gemv_b1_launch(const uint8_t* W, int64_t n, int64_t k, const float* 
   p.warps = warps;
   return launch_shape<kSoloWarps, false>(tmap, p, b1_smem_bytes(k, kSoloWarps), kSoloMaxSmem,
                                           pdl, s);
+}
+
+bool gemv_bm_supports(int64_t k, int64_t mb) {
+  return mb >= 2 && mb <= kMaxBatchRows &&
+         b1_smem_bytes(k, kPairWarps, static_cast<int>(mb)) <= kSoloMaxSmem;
+}
+
+int64_t gemv_bm_warps(int64_t units) {
+  const int64_t target = static_cast<int64_t>(sm_count()) * kPairWarps;
+  return units < target ? units : target;
+}
+
+cudaError_t gemv_bm_launch(const uint8_t* W, int64_t n, int64_t k, const float* x, int64_t mb,
+                           int64_t ldx, float* y, int64_t ldy, int32_t* counters,
+                           float* partials, int64_t units, int32_t* status, uint32_t flags,
+                           cudaStream_t s) {
+  if (!gemv_bm_supports(k, mb)) return cudaErrorInvalidValue;
+  CUtensorMap tmap;
+  if (!make_tmap(&tmap, W, n, k)) return cudaErrorInvalidValue;
+  const bool pdl = (flags & 1u) != 0;
+  B1Params p;
+  p.W = W;
+  p.n = n;
+  p.nsb = k / kSuperElems;
+  p.x = x;
+  p.y = y;
+  p.ldx = ldx;
+  p.ldy = ldy;
+  p.counters = counters;
+  p.partials = reinterpret_cast<uint64_t*>(partials);
+  p.units = units;
+  p.warps = gemv_bm_warps(units);
+  p.status = status;
+  p.flags = flags;
+  const size_t smem = b1_smem_bytes(k, kPairWarps, static_cast<int>(mb));
+  switch (mb) {
+    case 2: return pdl ? launch_batched<2, true>(tmap, p, smem, pdl, s)
+                       : launch_batched<2, false>(tmap, p, smem, pdl, s);
+    case 3: return pdl ? launch_batched<3, true>(tmap, p, smem, pdl, s)
+                       : launch_batched<3, false>(tmap, p, smem, pdl, s);
+    default: return pdl ? launch_batched<4, true>(tmap, p, smem, pdl, s)
+                        : launch_batched<4, false>(tmap, p, smem, pdl, s);
+  }
 }
 
 }  // namespace q4

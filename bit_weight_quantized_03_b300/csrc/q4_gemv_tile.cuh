@@ -76,6 +76,45 @@ __device__ __forceinline__ unsigned long long block_dot(const uint32_t (&r)[9],
   return acc;
 }
 
+// The same decode as block_dot without the products: dq[t] holds (q - 8) of
+// the element pair that block_dot multiplies by its activation pair xb[t], so
+// one decoded block can serve several rows of x.
+template <int BLK>
+__device__ __forceinline__ void block_decode(const uint32_t (&r)[9], const DecodeConsts& c,
+                                             unsigned long long (&dq)[16], float& d) {
+  if constexpr (BLK == 0) {
+    d = half_bits_to_float(r[0]);
+    {
+      const uint32_t w = r[0], t = shr12(w);
+      dq[0] = qm8<16, 12>(w, t, c);  // elements 0, 1
+      dq[8] = qm8<8, 16>(t, t, c);   // 16, 17
+    }
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+      const uint32_t w = r[1 + i], t = shr12(w);  // qs[2+4i .. 5+4i]
+      dq[1 + 2 * i] = qm8<0, 8>(w, w, c);        // 2+4i, 3+4i
+      dq[2 + 2 * i] = qm8<16, 12>(w, t, c);      // 4+4i, 5+4i
+      dq[9 + 2 * i] = qm8<4, 12>(w, w, c);       // 18+4i, 19+4i
+      dq[10 + 2 * i] = qm8<8, 16>(t, t, c);      // 20+4i, 21+4i
+    }
+    {
+      const uint32_t w = r[4];
+      dq[7] = qm8<0, 8>(w, w, c);    // 14, 15
+      dq[15] = qm8<4, 12>(w, w, c);  // 30, 31
+    }
+  } else {
+    d = half_bits_to_float(r[4] >> 16);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t w = r[5 + i], t = shr12(w);  // qs[4i .. 4i+3]
+      dq[2 * i] = qm8<0, 8>(w, w, c);            // 4i, 4i+1
+      dq[2 * i + 1] = qm8<16, 12>(w, t, c);      // 4i+2, 4i+3
+      dq[8 + 2 * i] = qm8<4, 12>(w, w, c);       // 4i+16, 4i+17
+      dq[9 + 2 * i] = qm8<8, 16>(t, t, c);       // 4i+18, 4i+19
+    }
+  }
+}
+
 __device__ __forceinline__ void lds_v2u64(uint32_t addr, unsigned long long& a,
                                           unsigned long long& b) {
   asm volatile("ld.shared.v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "r"(addr));
@@ -108,6 +147,45 @@ __device__ __forceinline__ void unit_dot(uint32_t slot, uint32_t xs, int sb, int
       float d;
       const f2 a = unpack2(b == 0 ? block_dot<0>(r, xb, dc, d) : block_dot<1>(r, xb, dc, d));
       yv[i] = fmaf(a.x + a.y, d, yv[i]);
+    }
+  }
+}
+
+// unit_dot for MB rows of x at once (MB small): every block of the lane's four
+// weight rows is decoded once and multiplied by the MB activation rows, which
+// are staged xrow bytes apart in shared memory; yv[m][i] accumulates row rr + 8i
+// of the group for activation row m.
+template <int MB>
+__device__ __forceinline__ void unit_dot_m(uint32_t slot, uint32_t xs, uint32_t xrow, int sb,
+                                           int j, int rr, const DecodeConsts& dc,
+                                           float (&yv)[MB][4]) {
+  const uint32_t src = slot + rr * kSuperBytes + 36 * j;
+  const int xe = sb * kSuperElems + 64 * j;  // first element of the pair
+#pragma unroll
+  for (int b = 0; b < 2; ++b) {
+    const uint32_t xa = xs + 4 * xpad_index(xe + 32 * b);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint32_t r[9];
+#pragma unroll
+      for (int w = 0; w < 5; ++w) r[4 * b + w] = lds32(src + i * 8 * kSuperBytes + 4 * (4 * b + w));
+      unsigned long long dq[16];
+      float d;
+      if (b == 0)
+        block_decode<0>(r, dc, dq, d);
+      else
+        block_decode<1>(r, dc, dq, d);
+#pragma unroll
+      for (int m = 0; m < MB; ++m) {
+        unsigned long long xb[16];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) lds_v2u64(xa + m * xrow + 16 * q, xb[2 * q], xb[2 * q + 1]);
+        unsigned long long acc = fmul2(dq[0], xb[0]);
+#pragma unroll
+        for (int t = 1; t < 16; ++t) acc = ffma2(dq[t], xb[t], acc);
+        const f2 a = unpack2(acc);
+        yv[m][i] = fmaf(a.x + a.y, d, yv[m][i]);
+      }
     }
   }
 }

@@ -31,6 +31,7 @@ cudaError_t f32_to_bf16_launch(const float* x, int64_t m, int64_t k, int64_t ldx
 struct GemvPlan {
   bool fast;          // streamed kernel (k % 256 == 0) vs the generic one
   bool b1;            // batch-1 streamed kernel (q4_gemv_b1.cu)
+  bool bm;            // 2..16 rows of x through the batched tile kernel, <= 4 per launch
   int64_t units;      // (32-row group, 256-wide k slice) pairs
   int64_t warps;      // workers the units are split over
   int64_t groups;     // 32-row groups
@@ -41,7 +42,16 @@ cudaError_t gemv_launch(const GemvPlan& plan, const uint8_t* W, int64_t n, int64
                         const float* x, int64_t m, int64_t ldx, float* y, int64_t ldy,
                         void* workspace, int32_t* status, uint32_t flags, cudaStream_t s);
 
+// Rows of x one batched tile launch carries (q4_gemv_b1.cu).
+constexpr int64_t kMaxBatchRows = 4;
+
 int64_t gemv_b1_warps(int64_t units);
+int64_t gemv_bm_warps(int64_t units);
+bool gemv_bm_supports(int64_t k, int64_t mb);
+cudaError_t gemv_bm_launch(const uint8_t* W, int64_t n, int64_t k, const float* x, int64_t mb,
+                           int64_t ldx, float* y, int64_t ldy, int32_t* counters,
+                           float* partials, int64_t units, int32_t* status, uint32_t flags,
+                           cudaStream_t s);
 bool gemv_b1_supports(int64_t k);
 cudaError_t gemv_b1_launch(const uint8_t* W, int64_t n, int64_t k, const float* x, float* y,
                            int32_t* counters, float* partials, int64_t units, int64_t warps,

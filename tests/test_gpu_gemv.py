@@ -39,9 +39,13 @@ def _gemv(torch, q4, W, n, k, x, **kw):
 
 # several tiles and ragged tails: n not a multiple of 32, k a multiple of 256
 # (streamed kernel) or only of 32 (generic kernel)
+# (several rows of x: launches of up to 4 rows of the batched tile kernel, 3
+# where 4 rows of x do not fit in shared memory (k = 9216, 10240), and a single
+# leftover row on the batch-1 kernel)
 SHAPES = [(1, 32, 1), (3, 288, 2), (4095, 256, 1), (33, 512, 3), (4096, 3072, 1),
           (1000, 3072, 4), (257, 9216, 1), (3072, 4096, 2), (96, 256, 16), (130, 1280, 8),
-          (64, 2304, 5), (1, 9216, 1), (2, 256, 9)]
+          (64, 2304, 5), (1, 9216, 1), (2, 256, 9), (1, 256, 2), (4096, 3072, 3),
+          (6144, 3072, 4), (257, 9216, 4), (100, 10240, 4), (3072, 9216, 7)]
 
 
 @pytest.mark.parametrize("n,k,m", SHAPES)
