@@ -455,6 +455,31 @@ def _run_gemm(args, world, dev, stream, bf16_burst, bf16_sust, peak_src, torch):
     return gemm
 
 
+def _fp32_fma_peak(dev, stream, torch):
+    """Measured fp32 FMA ceiling of this GPU: cuBLAS SGEMM 8192^3 with TF32 off
+    (a denominator only; nothing on the Q4 path uses it)."""
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = False
+    try:
+        g = torch.Generator(device=dev).manual_seed(11)
+        a = torch.randn((8192, 8192), device=dev, generator=g)
+        b = torch.randn((8192, 8192), device=dev, generator=g)
+        c = torch.empty((8192, 8192), device=dev)
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                torch.matmul(a, b, out=c)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(5):
+                torch.matmul(a, b, out=c)
+            e1.record(stream)
+        stream.synchronize()
+        secs = e0.elapsed_time(e1) * 1e-3 / 5
+        return 2 * 8192 ** 3 / secs / 1e12
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+
+
 def _run_crossover(args, dev, stream, hbm, bf16_burst, torch):
     """Batched decode on the 4096x3072 decoder shape: fp32 GEMV vs bf16 tensor-core
     GEMM for M in 1..128 concurrent streams, L2-cold (72 weight copies, 510 MB)."""
@@ -495,6 +520,10 @@ def _run_crossover(args, dev, stream, hbm, bf16_burst, torch):
                          "tflops": 2 * M * n * k / (us * 1e-6) / 1e12}
             del g
         rows[str(M)] = res
+    fp32_peak = _fp32_fma_peak(dev, stream, torch)
+    for r in rows.values():
+        if "gemv" in r:
+            r["gemv"]["frac_of_fp32_peak"] = r["gemv"]["tflops"] / fp32_peak
     cross = None
     for M in (1, 2, 4, 8, 16, 32, 64, 128):
         r = rows[str(M)]
@@ -504,7 +533,11 @@ def _run_crossover(args, dev, stream, hbm, bf16_burst, torch):
     return {"workload": "batched decode, 4096x3072 Q4_0, M concurrent streams, fp32 x (GEMV) / "
                         "bf16 x (tensor-core GEMM), fp32 y; 72 weight copies rotated (L2-cold)",
             "by_m": rows, "crossover_m": cross,
-            "note": "crossover_m = smallest M at which the tensor-core GEMM is faster"}
+            "fp32_peak_tflops": {"value": fp32_peak,
+                                 "source": "cuBLAS SGEMM 8192^3, TF32 off, measured in this run"},
+            "note": "crossover_m = smallest M at which the tensor-core GEMM is faster; "
+                    "gemv frac_of_fp32_peak = its 2*M*n*k flop rate over the measured fp32 "
+                    "FMA ceiling"}
 
 
 def main():
