@@ -524,22 +524,37 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int64_t tleft = args.m - m0;
           const int cnt = tleft < args.bn ? static_cast<int>(tleft) : args.bn;
           const int64_t split_stride = args.m * args.n;
-          for (int c = 0; c < cnt; c += 4) {  // four tokens at a time: independent loads
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            const float* pp = args.partials + (m0 + c) * args.n + grow;
-            for (int sp = 0; sp < args.splits; ++sp) {
+          // 16 tokens x 2 splits = 32 independent loads in flight per pass; the
+          // partials are still added in split order (deterministic)
+          constexpr int kT = 16;
+          for (int c = 0; c < cnt; c += kT) {
+            float acc[kT];
 #pragma unroll
-              for (int u = 0; u < 4; ++u)
-                if (c + u < cnt) acc[u] += __ldcg(pp + sp * split_stride + u * args.n);
+            for (int u = 0; u < kT; ++u) acc[u] = 0.f;
+            const float* pp = args.partials + (m0 + c) * args.n + grow;
+            for (int sp = 0; sp < args.splits; sp += 2) {
+              const bool two = sp + 1 < args.splits;
+              float v0[kT], v1[kT];
+#pragma unroll
+              for (int u = 0; u < kT; ++u) {
+                v0[u] = c + u < cnt ? __ldcg(pp + sp * split_stride + u * args.n) : 0.f;
+                v1[u] = (two && c + u < cnt) ? __ldcg(pp + (sp + 1) * split_stride + u * args.n)
+                                              : 0.f;
+              }
+#pragma unroll
+              for (int u = 0; u < kT; ++u) {
+                acc[u] += v0[u];
+                if (two) acc[u] += v1[u];
+              }
             }
             // the workspace goes back to all-zero, as every call leaves it
             for (int sp = 0; sp < args.splits; ++sp) {
 #pragma unroll
-              for (int u = 0; u < 4; ++u)
+              for (int u = 0; u < kT; ++u)
                 if (c + u < cnt) __stcg(const_cast<float*>(pp) + sp * split_stride + u * args.n, 0.f);
             }
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < kT; ++u) {
               if (c + u >= cnt) break;
               const int64_t tok = m0 + c + u;
               if (args.y_bf16)
