@@ -125,6 +125,27 @@ def test_workspace_sizes_are_consistent(q4):
     assert L.q4_linear_crossover_m(4096, 288) == q4.GEMV_MAX_M
 
 
+def test_gemv_workspace_covers_every_launch_of_a_batched_call(q4):
+    """A q4_gemv call with m >= 2 rows (k % 256 == 0) runs launches of up to 4
+    rows of the batched tile kernel (8 warps per SM) and, for a single leftover
+    row, the batch-1 kernel (up to 16 warps per SM).  Each warp of a launch may
+    publish one 64-bit word per row of x and output row of its 32-row group, so
+    the workspace must hold the per-group counters (rounded to 256 B) plus
+    warps x rows x 32 x 8 bytes for the largest launch.  Without a GPU the
+    library assumes 148 SMs."""
+    L = q4.lib()
+    sms = 148
+    for n, k in [(4096, 3072), (3072, 9216), (1000, 256), (131072, 3072), (33, 512)]:
+        groups = (n + 31) // 32
+        units = groups * (k // 256)
+        cnt = (groups * 4 + 255) // 256 * 256
+        for m in range(2, 17):
+            need = cnt + max(min(units, sms * 8) * min(m, 4) * 32 * 8,
+                             min(units, sms * 16) * 32 * 8 if m % 4 == 1 else 0)
+            got = L.q4_gemv_workspace_bytes(n, k, m)
+            assert got >= need, (n, k, m, got, need)
+
+
 def test_missing_library_fails_loudly(tmp_path, monkeypatch):
     import bit_weight_quantized_03_b300._lib as L
     monkeypatch.setattr(L, "_lib", None)
