@@ -113,6 +113,10 @@ q4_status q4_dequant_rows(const void* blocks, int64_t row0, int64_t n_rows, int6
  *   pass at least q4_gemv_workspace_bytes(n, k, m) bytes, 16-byte aligned
  *   (NULL is fine when that figure is 0).  Results do not depend on timing:
  *   the partial sums are added in a fixed order.
+ *   With k % 256 == 0 the call makes one launch per group of up to 4 rows of
+ *   x (each weight tile is decoded once for the rows of its launch), so the
+ *   weights are streamed ceil(m / 4) times; from m = 5 on the tensor-core
+ *   q4_gemm is the faster path (q4_linear_crossover_m).
  *   status_dev (may be NULL) receives Q4_ERR_TIMEOUT if a bounded wait ran out. */
 q4_status q4_gemv(const void* W, int64_t n, int64_t k, const float* x, int64_t m, int64_t ldx,
                   float* y, int64_t ldy, void* workspace, size_t ws_bytes, int32_t* status_dev,
