@@ -476,6 +476,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int64_t grow = n0 + 32 * q + lane;
       const bool split = args.splits > 1;
+      // 4-byte stores of bf16 pairs need an even row stride and a 4-byte base
+      const bool pair_stores =
+          (reinterpret_cast<uintptr_t>(args.y) & 3u) == 0 && (args.ldy & 1) == 0;
 #pragma unroll 1
       for (int c0 = 0; c0 < args.bn; c0 += 32) {
         uint32_t v[32];
@@ -486,9 +489,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(B.acc_empty + 8 * b);
         }
-        if (grow < args.n) {
-          const int64_t tleft = args.m - (m0 + c0);
-          const int cnt = tleft < 32 ? static_cast<int>(tleft) : 32;
+        const int64_t tleft = args.m - (m0 + c0);
+        const int cnt = tleft < 32 ? static_cast<int>(tleft) : 32;
+        if (!split && args.y_bf16 && pair_stores) {
+          // bf16 Y: lanes 2i and 2i + 1 (rows r0, r0 + 1) swap one value per
+          // token pair, so each lane stores one 4-byte bf16 pair: the even
+          // lane rows (r0, r0 + 1) of token j, the odd lane those of token
+          // j + 1.  Warp-uniform branch: every lane takes part in the shuffle.
+          const bool odd = (lane & 1) != 0;
+          const int64_t r0 = grow - (odd ? 1 : 0);
+          __nv_bfloat16* yb = static_cast<__nv_bfloat16*>(args.y);
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            const float own_j = __uint_as_float(v[j]), own_j1 = __uint_as_float(v[j + 1]);
+            const float recv = __shfl_xor_sync(0xffffffffu, odd ? own_j : own_j1, 1);
+            const int tj = odd ? j + 1 : j;
+            if (tj < cnt && r0 < args.n) {
+              const float lo = odd ? recv : own_j;   // row r0
+              const float hi = odd ? own_j1 : recv;  // row r0 + 1
+              __nv_bfloat16* p = yb + (m0 + c0 + tj) * args.ldy + r0;
+              if (r0 + 1 < args.n)
+                *reinterpret_cast<uint32_t*>(p) = bf16x2_rn(lo, hi);
+              else
+                *p = __float2bfloat16_rn(lo);
+            }
+          }
+        } else if (grow < args.n) {
           if (split) {  // this K-split's partial tile, fp32
             float* pp = args.partials + (static_cast<int64_t>(it.split) * args.m + m0 + c0) *
                                             args.n + grow;

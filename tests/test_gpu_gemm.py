@@ -46,14 +46,29 @@ def test_gemm_matches_oracle(torch, q4, oracle_mod, n, k, m):
     assert ok, info
 
 
-def test_gemm_bf16_output(torch, q4, oracle_mod):
-    n, k, m = 640, 1280, 100
-    W, xb = _case(torch, oracle_mod, n, k, m, seed=9)
+# bf16 Y: even row strides take the paired 4-byte stores of the epilogue
+# (odd n cuts a pair at the matrix edge, odd m a token pair at the tail); an
+# odd row stride (pad 1) takes the 2-byte stores.  Padding must stay untouched.
+@pytest.mark.parametrize("n,k,m,pad", [(640, 1280, 100, 0), (333, 512, 37, 0),
+                                       (200, 512, 65, 1), (129, 256, 3, 2)])
+def test_gemm_bf16_output(torch, q4, oracle_mod, n, k, m, pad):
+    W, xb = _case(torch, oracle_mod, n, k, m, seed=9 + n + pad)
     Y, S = oracle_mod.matmul(W, n, k, xb.float().numpy())
-    got = q4.q4_gemm(torch.from_numpy(W).cuda(), n, k, xb.cuda(), y_dtype=torch.bfloat16)
-    assert got.dtype == torch.bfloat16
-    ok, info = within_tol(got.float().cpu().numpy(), Y, S, TOL)
+    Yd = torch.full((m, n + pad), 7.0, dtype=torch.bfloat16, device="cuda")
+    q4.q4_gemm(torch.from_numpy(W).cuda(), n, k, xb.cuda(), Y=Yd[:, :n])
+    got = Yd.float().cpu().numpy()
+    ok, info = within_tol(got[:, :n], Y, S, TOL)
     assert ok, info
+    assert np.all(got[:, n:] == 7.0)
+
+
+def test_gemm_unit_rows_give_bf16_columns_in_bf16(torch, q4, oracle_mod):
+    n, k = 201, 256
+    W, _ = _case(torch, oracle_mod, n, k, 1, seed=6)
+    cols = oracle_mod.dequant_rows(W, n, k).T  # [k, n], exact fp32
+    X = torch.eye(k, dtype=torch.bfloat16)
+    got = q4.q4_gemm(torch.from_numpy(W).cuda(), n, k, X.cuda(), y_dtype=torch.bfloat16)
+    assert np.array_equal(got.float().cpu().numpy(), bf16_round(cols))
 
 
 def test_gemm_unit_rows_give_bf16_columns(torch, q4, oracle_mod):
