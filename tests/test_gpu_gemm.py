@@ -46,11 +46,12 @@ def test_gemm_matches_oracle(torch, q4, oracle_mod, n, k, m):
     assert ok, info
 
 
-# bf16 Y: even row strides take the paired 4-byte stores of the epilogue
-# (odd n cuts a pair at the matrix edge, odd m a token pair at the tail); an
-# odd row stride (pad 1) takes the 2-byte stores.  Padding must stay untouched.
-@pytest.mark.parametrize("n,k,m,pad", [(640, 1280, 100, 0), (333, 512, 37, 0),
-                                       (200, 512, 65, 1), (129, 256, 3, 2)])
+# bf16 Y: even row strides take the epilogue's 4-byte stores of row pairs,
+# odd strides 2-byte stores; n and m ragged so that an edge row pair and a tail
+# token pair are cut.  Padding must stay untouched.
+@pytest.mark.parametrize("n,k,m,pad", [(640, 1280, 100, 0), (334, 512, 37, 2),
+                                       (129, 256, 3, 3), (333, 512, 37, 1),
+                                       (333, 512, 37, 0), (200, 512, 65, 1)])
 def test_gemm_bf16_output(torch, q4, oracle_mod, n, k, m, pad):
     W, xb = _case(torch, oracle_mod, n, k, m, seed=9 + n + pad)
     Y, S = oracle_mod.matmul(W, n, k, xb.float().numpy())
@@ -62,8 +63,9 @@ def test_gemm_bf16_output(torch, q4, oracle_mod, n, k, m, pad):
     assert np.all(got[:, n:] == 7.0)
 
 
-def test_gemm_unit_rows_give_bf16_columns_in_bf16(torch, q4, oracle_mod):
-    n, k = 201, 256
+@pytest.mark.parametrize("n", [201, 202, 204])
+def test_gemm_unit_rows_give_bf16_columns_in_bf16(torch, q4, oracle_mod, n):
+    k = 256
     W, _ = _case(torch, oracle_mod, n, k, 1, seed=6)
     cols = oracle_mod.dequant_rows(W, n, k).T  # [k, n], exact fp32
     X = torch.eye(k, dtype=torch.bfloat16)
