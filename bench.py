@@ -221,6 +221,31 @@ def _time_graph_replays(graphs, stream, torch):
     return e0.elapsed_time(e1)
 
 
+def _region_count(est_ms: float, world: int, torch, min_regions: int = 5,
+                  min_total_ms: float = 500.0, max_regions: int = 200) -> int:
+    """How many timed regions of K steps to run: at least `min_regions` and
+    enough to cover `min_total_ms`; the same count on every rank."""
+    n = max(min_regions, int(min_total_ms / max(est_ms, 1e-3)) + 1)
+    n = min(n, max_regions)
+    return int(_barrier_max(float(n), world, torch))
+
+
+def _timed_regions(fn, regions: int, world: int, dev, torch):
+    """Run `fn` (one timed region, returns device ms) `regions` times, each
+    bracketed by a barrier and a synchronize, with the clocks sampled across
+    all of them; returns ((max over ranks of the median ms, stats), clocks)."""
+    times = []
+    with ClockSampler(dev.index) as clk:
+        for _ in range(regions):
+            torch.cuda.synchronize()
+            _barrier(world)
+            torch.cuda.synchronize()
+            times.append(fn())
+            torch.cuda.synchronize()
+    med = _barrier_max(statistics.median(times), world, torch)
+    return (med, {"regions": regions, "min_ms": min(times), "max_ms": max(times)}), clk.summary()
+
+
 def run_ours(args):
     import torch
 
@@ -247,8 +272,10 @@ def run_ours(args):
     if args.only in ("all", "stack"):
         line.update(_run_stack(args, world, dev, stream, hbm, peak_src, torch))
     extra = {}
+    if args.only in ("all", "single"):
+        extra["single_gemv"] = _run_single_gemv(args, dev, stream, hbm, torch)
     if args.only in ("all", "head", "gather"):
-        extra = _run_head_gather(args, dev, stream, hbm, torch)
+        extra.update(_run_head_gather(args, dev, stream, hbm, torch))
     gemm = None
     if args.only in ("all", "gemm"):
         gemm = _run_gemm(args, world, dev, stream, bf16_burst, bf16_sust, peak_src, torch)
@@ -289,20 +316,22 @@ def _run_stack(args, world, dev, stream, hbm, peak_src, torch):
         def plan(steps):
             return [(g_multi, steps // G), (g_one, steps % G)]
 
-        _time_graph_replays(plan(max(args.warmup, 3)), stream, torch)
+        # Warm-up: every graph that the timed region replays is replayed here
+        # first (a graph's first replay uploads it), whatever --warmup is.
+        _time_graph_replays([(g_multi, max(1, args.warmup // G)),
+                             (g_one, max(1, args.warmup % G))], stream, torch)
         torch.cuda.synchronize()
-        _barrier(world)
-        torch.cuda.synchronize()
-        with ClockSampler(dev.index) as clk:
-            ms = _time_graph_replays(plan(args.steps), stream, torch)
-        torch.cuda.synchronize()
-        return _barrier_max(ms, world, torch), clk.summary()
+        est = _time_graph_replays(plan(args.steps), stream, torch)
+        regions = _region_count(est, world, torch)
+        return _timed_regions(lambda: _time_graph_replays(plan(args.steps), stream, torch),
+                              regions, world, dev, torch)
 
-    ms_chain, clocks_chain = timed(chain=True)
-    ms_pl, clocks_pl = timed(chain=False)
+    (ms_chain, reg_chain), clocks_chain = timed(chain=True)
+    (ms_pl, reg_pl), clocks_pl = timed(chain=False)
     # headline: the faster of the two ways of running the same step
     use_chain = ms_chain < ms_pl
-    ms, clocks = (ms_chain, clocks_chain) if use_chain else (ms_pl, clocks_pl)
+    ms, clocks, reg = ((ms_chain, clocks_chain, reg_chain) if use_chain else
+                       (ms_pl, clocks_pl, reg_pl))
     ms_step = ms / args.steps
     value = world * wbytes * args.steps / (ms * 1e-3) / 1e9
     achieved = (wbytes + abytes) / (ms_step * 1e-3) / 1e9
@@ -320,18 +349,24 @@ def _run_stack(args, world, dev, stream, hbm, peak_src, torch):
             g_e2e.replay()
             y_host[s:s + 1].copy_(dec.x, non_blocking=True)
     stream.synchronize()
-    _barrier(world)
-    t0 = time.perf_counter()
-    with torch.cuda.stream(stream):
-        for s in range(args.steps):
-            x_dev.copy_(x_host[s:s + 1], non_blocking=True)
-            g_e2e.replay()
-            y_host[s:s + 1].copy_(dec.x, non_blocking=True)
-    stream.synchronize()
-    e2e_s = _barrier_max(time.perf_counter() - t0, world, torch)
+
+    def e2e_region():
+        _barrier(world)
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            for s in range(args.steps):
+                x_dev.copy_(x_host[s:s + 1], non_blocking=True)
+                g_e2e.replay()
+                y_host[s:s + 1].copy_(dec.x, non_blocking=True)
+        stream.synchronize()
+        return (time.perf_counter() - t0) * 1e3
+
+    e2e_times = [e2e_region() for _ in range(reg["regions"])]
+    e2e_s = _barrier_max(statistics.median(e2e_times), world, torch) * 1e-3
     e2e = {"value": world * wbytes * args.steps / e2e_s / 1e9, "unit": "GB/s",
            "h2d_bytes_per_step": 3072 * 4, "d2h_bytes_per_step": 3072 * 4,
-           "ms_per_step": e2e_s / args.steps * 1e3}
+           "ms_per_step": e2e_s / args.steps * 1e3,
+           "timing": f"host clock, median of {reg['regions']} regions of {args.steps} steps"}
     del g_e2e
     return {
         "value": value, "ms_per_step": ms_step,
@@ -339,6 +374,11 @@ def _run_stack(args, world, dev, stream, hbm, peak_src, torch):
                    "gqa": "32Q/8KV", "ffn": 9216, "batch": 1,
                    "weight_bytes_per_step": wbytes, "activation_bytes_per_step": abytes,
                    "l2": "inputs larger than L2: 1.70 GB of weights per step vs 126 MB L2",
+                   "timing": (f"CUDA events on the launching stream; median of "
+                              f"{reg['regions']} timed regions of exactly {args.steps} steps "
+                              f"(min {reg['min_ms'] / args.steps:.4f}, max "
+                              f"{reg['max_ms'] / args.steps:.4f} ms/step), each bracketed by a "
+                              f"barrier and synchronize; every graph replayed before timing"),
                    "graph": (f"CUDA graphs of {G} steps, " +
                              ("one q4_gemv_chain launch per step" if use_chain else
                               "104 q4_gemv launches per step with programmatic dependent launch")),
@@ -362,6 +402,45 @@ def _run_stack(args, world, dev, stream, hbm, peak_src, torch):
         "gpu_launches": args.steps * (1 if use_chain else dec.launches_per_step()),
         "clocks": clocks,
     }
+
+
+def _run_single_gemv(args, dev, stream, hbm, torch):
+    """Single batch-1 GEMV on the 4096 x 3072 decoder shape: Q4_0 weights
+    N(0, 0.02^2), x N(0, 1) fp32, y fp32.  L2-cold: 36 distinct weight copies
+    (255 MB, twice the L2) are rotated, 72 calls per CUDA graph."""
+    import synth
+    from bit_weight_quantized_03_b300 import FLAG_PDL, Workspace, q4_gemv, q4_quantize
+    n, k, copies, reps = 4096, 3072, 36, 72
+    Ws = []
+    for c in range(copies):
+        w = synth.torch_weights(n, k, seed=synth.seed_for(1, 0, c), device=dev)
+        Ws.append(q4_quantize(w))
+        del w
+    x = synth.torch_activations(1, k, seed=synth.activation_seed(1000), device=dev)
+    y = torch.empty((1, n), device=dev)
+    ws = Workspace(dev)
+    algo = n * k // 32 * 18 + 4 * (k + n)
+    out = {"workload": "single Q4_0 GEMV 4096x3072, batch 1, fp32 x and y",
+           "algorithmic_bytes_per_call": algo,
+           "l2": f"{copies} weight copies rotated ({copies * n * k // 32 * 18 / 1e6:.0f} MB)"}
+    for name, flags in (("q4_gemv_pdl", FLAG_PDL), ("q4_gemv", 0)):
+        with torch.cuda.stream(stream):
+            q4_gemv(Ws[0], n, k, x, y=y, workspace=ws, stream=stream)
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(reps):
+                    q4_gemv(Ws[i % copies], n, k, x, y=y, workspace=ws, flags=flags,
+                            stream=stream)
+        _time_graph_replays([(g, 2)], stream, torch)
+        us = statistics.median(_time_graph_replays([(g, 1)], stream, torch) for _ in range(7)) \
+            / reps * 1e3
+        out[name] = {"us_per_call": us, "gbs": algo / (us * 1e-6) / 1e9,
+                     "frac_of_hbm": algo / (us * 1e-6) / 1e9 / hbm}
+        del g
+    best = min((v["us_per_call"], key) for key, v in out.items() if isinstance(v, dict))
+    out["best"] = best[1]
+    return out
 
 
 def _run_head_gather(args, dev, stream, hbm, torch):
@@ -546,7 +625,8 @@ def main():
     ap.add_argument("--steps", type=int, default=256)
     ap.add_argument("--warmup", type=int, default=16)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--only", choices=["all", "stack", "head", "gather", "gemm", "crossover"],
+    ap.add_argument("--only", choices=["all", "stack", "single", "head", "gather", "gemm",
+                                       "crossover"],
                     default="all",
                     help="run one section (profiling runs); the default runs all of them")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)

@@ -43,7 +43,35 @@ q4_status check_matrix(const void* W, int64_t n, int64_t k) {
   return Q4_OK;
 }
 
+// Every argument rule of q4_gemm that the host can check (the workspace aside).
+q4_status gemm_check_args(const void* W, int64_t n, int64_t k, const void* X, int64_t m,
+                          int64_t ldx, const void* Y, q4_dtype y_dtype, int64_t ldy) {
+  q4_status st = check_matrix(W, n, k);
+  if (st != Q4_OK) return st;
+  if (X == nullptr || Y == nullptr || m <= 0 || m > kMaxDim || ldx < k || ldy < n)
+    return Q4_ERR_INVALID_ARG;
+  if (y_dtype != Q4_F32 && y_dtype != Q4_BF16) return Q4_ERR_INVALID_ARG;
+  if (k % 256 != 0) return Q4_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(X, 16) || ldx % 8 != 0) return Q4_ERR_MISALIGNED;
+  if (!aligned(Y, y_dtype == Q4_F32 ? 4 : 2)) return Q4_ERR_MISALIGNED;
+  return Q4_OK;
+}
+
 }  // namespace
+
+namespace q4 {
+
+q4_status gemv_check_args(const void* W, int64_t n, int64_t k, const float* x, int64_t m,
+                          int64_t ldx, const float* y, int64_t ldy) {
+  q4_status st = check_matrix(W, n, k);
+  if (st != Q4_OK) return st;
+  if (x == nullptr || y == nullptr || m <= 0 || ldx < k || ldy < n) return Q4_ERR_INVALID_ARG;
+  if (m > Q4_GEMV_MAX_M) return Q4_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(x, 16) || ldx % 4 != 0 || !aligned(y, 4)) return Q4_ERR_MISALIGNED;
+  return Q4_OK;
+}
+
+}  // namespace q4
 
 extern "C" {
 
@@ -94,11 +122,8 @@ size_t q4_gemv_workspace_bytes(int64_t n, int64_t k, int64_t m) {
 q4_status q4_gemv(const void* W, int64_t n, int64_t k, const float* x, int64_t m, int64_t ldx,
                   float* y, int64_t ldy, void* workspace, size_t ws_bytes, int32_t* status_dev,
                   uint32_t flags, q4_stream_t s) {
-  q4_status st = check_matrix(W, n, k);
+  q4_status st = q4::gemv_check_args(W, n, k, x, m, ldx, y, ldy);
   if (st != Q4_OK) return st;
-  if (x == nullptr || y == nullptr || m <= 0 || ldx < k || ldy < n) return Q4_ERR_INVALID_ARG;
-  if (m > Q4_GEMV_MAX_M) return Q4_ERR_UNSUPPORTED_SHAPE;
-  if (!aligned(x, 16) || ldx % 4 != 0 || !aligned(y, 4)) return Q4_ERR_MISALIGNED;
   const q4::GemvPlan plan = q4::gemv_plan(n, k, m);
   if (plan.ws_bytes > 0 && (workspace == nullptr || ws_bytes < plan.ws_bytes))
     return Q4_ERR_WORKSPACE;
@@ -115,14 +140,8 @@ size_t q4_gemm_workspace_bytes(int64_t n, int64_t k, int64_t m) {
 q4_status q4_gemm(const void* W, int64_t n, int64_t k, const void* X, int64_t m, int64_t ldx,
                   void* Y, q4_dtype y_dtype, int64_t ldy, void* workspace, size_t ws_bytes,
                   int32_t* status_dev, uint32_t flags, q4_stream_t s) {
-  q4_status st = check_matrix(W, n, k);
+  q4_status st = gemm_check_args(W, n, k, X, m, ldx, Y, y_dtype, ldy);
   if (st != Q4_OK) return st;
-  if (X == nullptr || Y == nullptr || m <= 0 || m > kMaxDim || ldx < k || ldy < n)
-    return Q4_ERR_INVALID_ARG;
-  if (y_dtype != Q4_F32 && y_dtype != Q4_BF16) return Q4_ERR_INVALID_ARG;
-  if (k % 256 != 0) return Q4_ERR_UNSUPPORTED_SHAPE;
-  if (!aligned(X, 16) || ldx % 8 != 0) return Q4_ERR_MISALIGNED;
-  if (!aligned(Y, y_dtype == Q4_F32 ? 4 : 2)) return Q4_ERR_MISALIGNED;
   const q4::GemmPlan plan = q4::gemm_plan(n, k, m);
   if (plan.ws_bytes > 0 && (workspace == nullptr || ws_bytes < plan.ws_bytes))
     return Q4_ERR_WORKSPACE;
@@ -264,12 +283,18 @@ q4_status q4_linear(const void* W, int64_t n, int64_t k, const void* X, q4_dtype
                    status_dev, flags, s);
   if (x_dtype == Q4_BF16)
     return q4_gemm(W, n, k, X, m, ldx, Y, Q4_F32, ldy, workspace, ws_bytes, status_dev, flags, s);
-  // fp32 activations on the tensor-core path: round them to bf16 first
+  // fp32 activations on the tensor-core path: round them to bf16 into the
+  // workspace first.  Every rule q4_gemm will apply to that call is checked
+  // here, before the conversion is launched, so that a refused call launches
+  // nothing and leaves the workspace as it was.
   if (!aligned(X, 16) || ldx % 4 != 0) return Q4_ERR_MISALIGNED;
+  const size_t gemm_ws = (q4_gemm_workspace_bytes(n, k, m) + 255) / 256 * 256;
+  void* xb = workspace == nullptr ? nullptr : static_cast<uint8_t*>(workspace) + gemm_ws;
+  st = gemm_check_args(W, n, k, X, m, k, Y, Q4_F32, ldy);
+  if (st != Q4_OK) return st;
   const size_t need = q4_linear_workspace_bytes(n, k, m, x_dtype);
   if (workspace == nullptr || ws_bytes < need) return Q4_ERR_WORKSPACE;
-  const size_t gemm_ws = (q4_gemm_workspace_bytes(n, k, m) + 255) / 256 * 256;
-  void* xb = static_cast<uint8_t*>(workspace) + gemm_ws;
+  if (!aligned(workspace, 16)) return Q4_ERR_MISALIGNED;
   cudaError_t e = q4::f32_to_bf16_launch(static_cast<const float*>(X), m, k, ldx, xb, k,
                                          reinterpret_cast<cudaStream_t>(s));
   if (e != cudaSuccess) return Q4_ERR_CUDA;

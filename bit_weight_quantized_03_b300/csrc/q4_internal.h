@@ -8,6 +8,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "../../include/q4.h"
+
 namespace q4 {
 
 // Wall-clock limit of every bounded wait inside a kernel (nanoseconds).
@@ -28,6 +30,11 @@ cudaError_t f32_to_bf16_launch(const float* x, int64_t m, int64_t k, int64_t ldx
                                int64_t ldo, cudaStream_t s);
 
 // --------------------------------------------------------------- GEMV
+// The host-side argument rules of q4_gemv (matrix, x, y, m, leading
+// dimensions, alignment); Q4_OK or the status q4_gemv would return.
+q4_status gemv_check_args(const void* W, int64_t n, int64_t k, const float* x, int64_t m,
+                          int64_t ldx, const float* y, int64_t ldy);
+
 struct GemvPlan {
   bool fast;          // streamed kernel (k % 256 == 0) vs the generic one
   bool b1;            // batch-1 streamed kernel (q4_gemv_b1.cu)

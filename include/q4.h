@@ -22,8 +22,10 @@
  *
  * Conventions shared by every call.
  *   - Pointers are DEVICE pointers owned by the caller, unless a call says
- *     otherwise.  The library keeps no allocation of its own; scratch space is
- *     passed in as `workspace`.
+ *     otherwise.  Scratch space is passed in as `workspace`; the one
+ *     exception is q4_gemv_noalloc, whose scratch is a fixed array of
+ *     Q4_GEMV_NOALLOC_SCRATCH_BYTES that the library holds in device memory
+ *     of every GPU that loads it.  The library allocates nothing else.
  *   - Every call is asynchronous on stream `s` (NULL = the legacy default
  *     stream) and never synchronizes the host.
  *   - Errors the host can see (null pointer, bad size, k % 32 != 0, broken
@@ -139,7 +141,9 @@ size_t q4_gemv_workspace_bytes(int64_t n, int64_t k, int64_t m);
  * device address with that device current: make it before any stream
  * capture.  All calls share the array, so calls that may overlap on the GPU
  * (other streams, other host threads) race and give wrong results; serialise
- * them on one stream. */
+ * them on one stream.  The address is cached per CUDA context, so the first
+ * call in a new context (after cudaDeviceReset, say) looks it up again and
+ * must also come before any capture. */
 #define Q4_GEMV_NOALLOC_SCRATCH_BYTES 4194304 /* 4 MiB */
 q4_status q4_gemv_noalloc(const void* W, int64_t n, int64_t k, const float* x, int64_t m,
                           int64_t ldx, float* y, int64_t ldy, int32_t* status_dev,

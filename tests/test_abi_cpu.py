@@ -111,6 +111,15 @@ def test_host_validation_rejects_bad_arguments(q4):
     assert L.q4_gemm(A16, 8, 256, A16, 4, 256, A16, 5, 8, None, 0, None, 0, None) == q4.ERR_INVALID_ARG
     # linear: bad dtype
     assert L.q4_linear(A16, 8, 256, A16, 3, 4, 256, A16, 8, None, 0, None, 0, None) == q4.ERR_INVALID_ARG
+    # linear, fp32 X beyond the GEMV batch with k % 256 != 0: the tensor-core
+    # path cannot take k, and the call is refused before the bf16 conversion
+    # (the fake addresses are never dereferenced; no CUDA call is made)
+    assert L.q4_linear(A16, 8, 3104, A16, 0, 17, 3104, A16, 8, A16, 1 << 30, None, 0,
+                       None) == q4.ERR_UNSUPPORTED_SHAPE
+    # noalloc: every q4_gemv rule is applied before anything touches the device
+    assert L.q4_gemv_noalloc(A16, 8, 64, A16, 1, 32, A16, 8, None, 0, None) == q4.ERR_INVALID_ARG
+    assert L.q4_gemv_noalloc(A16, 8, 64, A2, 1, 64, A16, 8, None, 0, None) == q4.ERR_MISALIGNED
+    assert L.q4_gemv_noalloc(A16, 8, 64, A16, 2, 66, A16, 8, None, 0, None) == q4.ERR_MISALIGNED
 
 
 def test_workspace_sizes_are_consistent(q4):

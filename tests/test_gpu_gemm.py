@@ -155,3 +155,19 @@ def test_gemm_split_k_leaves_workspace_zero(torch, q4, oracle_mod):
     Y, S = oracle_mod.matmul(W, n, k, xb.float().cpu().numpy())
     ok, info = within_tol(y.cpu().numpy(), Y, S, 8e-3)
     assert ok, info
+
+
+def test_linear_refused_tensor_core_call_launches_nothing(torch, q4):
+    """fp32 X with m above the GEMV batch and k % 256 != 0 cannot run on the
+    tensor cores: the call is refused before the fp32 -> bf16 conversion is
+    launched, so the shared workspace stays all zero for the next GEMV."""
+    n, k, m = 64, 3104, 17
+    W = torch.zeros((n, k // 32 * 18), dtype=torch.uint8, device="cuda")
+    x = torch.ones((m, k), dtype=torch.float32, device="cuda")
+    y = torch.zeros((m, n), dtype=torch.float32, device="cuda")
+    ws = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
+    st = q4.lib().q4_linear(W.data_ptr(), n, k, x.data_ptr(), q4.F32, m, k, y.data_ptr(), n,
+                            ws.data_ptr(), ws.numel(), None, 0, None)
+    torch.cuda.synchronize()
+    assert st == q4.ERR_UNSUPPORTED_SHAPE
+    assert int(ws.count_nonzero().item()) == 0

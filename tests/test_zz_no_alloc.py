@@ -6,14 +6,17 @@ streaming has started, a plugin handed only its input and output buffers).
 Its split-K scratch is one fixed array inside the library, shared by every
 call, so the test makes several calls in a row -- different shapes, so that a
 call that started from the previous call's leftovers would show -- and checks
-each against the existing q4_gemv entry point (its own zero-filled workspace)
-within the GEMV tolerance |y - y_ref| <= 1e-4 * sum_j |w^ x| (sum from the CPU
-oracle).  This file is collected last on purpose.
+each element-wise against the CPU oracle's fp64 product and against the
+existing q4_gemv entry point (its own zero-filled workspace), within the GEMV
+tolerance |y - y_ref| <= 1e-4 * sum_j |w^ x|; then a call whose bounded wait
+runs out is followed by a normal call that must be correct with no reset.
+This file is collected last on purpose.
 """
 import numpy as np
 import pytest
 
 import synth
+from gpu_helpers import within_tol
 
 pytestmark = pytest.mark.gpu
 TOL = 1e-4
@@ -36,13 +39,18 @@ def q4():
     return m
 
 
-def test_noalloc_matches_q4_gemv_on_calls_in_a_row(torch, q4, oracle_mod):
+def _case(oracle_mod, n, k, m, seed):
+    w = synth.np_weights(n, k, seed=seed)
+    x = synth.np_activations(m, k, seed=seed + 50)
+    W, rc, _ = oracle_mod.quantize(w)
+    assert rc == 0
+    Y, S = oracle_mod.matmul(W, n, k, x, nthreads=oracle_mod.cpu_count())
+    return W, x, Y, S
+
+
+def test_noalloc_matches_oracle_and_q4_gemv_on_calls_in_a_row(torch, q4, oracle_mod):
     for i, (n, k, m) in enumerate(CALLS):
-        w = synth.np_weights(n, k, seed=900 + i)
-        x = synth.np_activations(m, k, seed=950 + i)
-        W, rc, _ = oracle_mod.quantize(w)
-        assert rc == 0
-        _, S = oracle_mod.matmul(W, n, k, x, nthreads=oracle_mod.cpu_count())
+        W, x, Y, S = _case(oracle_mod, n, k, m, seed=900 + i)
         Wd, xd = torch.from_numpy(W).cuda(), torch.from_numpy(x).cuda()
         y_ref = q4.q4_gemv(Wd, n, k, xd, workspace=q4.Workspace()).cpu().numpy()
         # output and status word allocated before the call: the call itself allocates nothing
@@ -51,8 +59,32 @@ def test_noalloc_matches_q4_gemv_on_calls_in_a_row(torch, q4, oracle_mod):
         q4.q4_gemv_noalloc(Wd, n, k, xd, y=y, status=st)
         torch.cuda.synchronize()
         assert int(st.item()) == 0
-        err = np.abs(y.cpu().numpy().astype(np.float64) - y_ref.astype(np.float64))
+        got = y.cpu().numpy()
+        ok, info = within_tol(got, Y, S, TOL)  # element-wise against the fp64 oracle
+        assert ok, (i, n, k, m, info)
+        err = np.abs(got.astype(np.float64) - y_ref.astype(np.float64))
         assert np.all(err <= TOL * S), (i, n, k, m, float(np.max(err / np.maximum(S, 1e-30))))
+
+
+def test_noalloc_call_after_a_timed_out_call(torch, q4, oracle_mod):
+    """A call whose bounded wait runs out (test flag) may leave partial sums in
+    the shared scratch; the next call clears what it uses, so it is correct
+    without any reset by the caller."""
+    n, k, m = 4096, 3072, 1
+    W, x, Y, S = _case(oracle_mod, n, k, m, seed=990)
+    Wd, xd = torch.from_numpy(W).cuda(), torch.from_numpy(x).cuda()
+    y = torch.zeros((m, n), dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    q4.q4_gemv_noalloc(Wd, n, k, xd, y=y, status=st, flags=q4.FLAG_TEST_STALL)
+    torch.cuda.synchronize()
+    assert int(st.item()) == q4.ERR_TIMEOUT
+    st.zero_()
+    y.fill_(float("nan"))
+    q4.q4_gemv_noalloc(Wd, n, k, xd, y=y, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ok, info = within_tol(y.cpu().numpy(), Y, S, TOL)
+    assert ok, info
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch(q4):
