@@ -77,6 +77,19 @@ def lib():
             L.q4o_matmul.restype = ctypes.c_int
             L.q4o_embed_gather.argtypes = [u8p, i64, i64, i32p, i64, f32p]
             L.q4o_embed_gather.restype = ctypes.c_int
+            L.q4o_matmul_f64.argtypes = [u8p, i64, i64, f64p, i64, i64, f64p, f64p, i64,
+                                         ctypes.c_int]
+            L.q4o_matmul_f64.restype = ctypes.c_int
+            L.q4o_swiglu.argtypes = [f64p, f64p, i64, f64p]
+            L.q4o_swiglu.restype = None
+            L.q4o_argmax.argtypes = [f64p, i64]
+            L.q4o_argmax.restype = i64
+            L.q4o_repack_bytes.argtypes = [i64, i64]
+            L.q4o_repack_bytes.restype = i64
+            L.q4o_repack.argtypes = [u8p, i64, i64, u8p]
+            L.q4o_repack.restype = ctypes.c_int
+            L.q4o_unrepack.argtypes = [u8p, i64, i64, u8p]
+            L.q4o_unrepack.restype = ctypes.c_int
             _lib = L
     return _lib
 
@@ -152,6 +165,63 @@ def matmul(W: np.ndarray, n: int, k: int, X: np.ndarray, nthreads: int = 1):
     if rc != OK:
         raise ValueError("q4o_matmul: invalid arguments")
     return Y, S
+
+
+def matmul_f64(W: np.ndarray, n: int, k: int, X: np.ndarray):
+    """As matmul, with X taken in fp64 exactly as given."""
+    W = _blocks(W, n, k)
+    X = np.ascontiguousarray(np.atleast_2d(X), dtype=np.float64)
+    m = X.shape[0]
+    if X.shape[1] != k:
+        raise ValueError("X has the wrong width")
+    Y = np.empty((m, n), np.float64)
+    S = np.empty((m, n), np.float64)
+    rc = lib().q4o_matmul_f64(_ptr(W, ctypes.c_uint8), n, k, _ptr(X, ctypes.c_double), m, k,
+                              _ptr(Y, ctypes.c_double), _ptr(S, ctypes.c_double), n, 1)
+    if rc != OK:
+        raise ValueError("q4o_matmul_f64: invalid arguments")
+    return Y, S
+
+
+def swiglu(a, b) -> np.ndarray:
+    """fp64 SiLU-gated unit a * sigmoid(a) * b (the gated FFN activation reading)."""
+    a = np.ascontiguousarray(a, dtype=np.float64).ravel()
+    b = np.ascontiguousarray(b, dtype=np.float64).ravel()
+    if a.size != b.size:
+        raise ValueError("a and b differ in size")
+    out = np.empty(a.size, np.float64)
+    lib().q4o_swiglu(_ptr(a, ctypes.c_double), _ptr(b, ctypes.c_double), a.size,
+                     _ptr(out, ctypes.c_double))
+    return out
+
+
+def argmax(y) -> int:
+    y = np.ascontiguousarray(y, dtype=np.float64).ravel()
+    return int(lib().q4o_argmax(_ptr(y, ctypes.c_double), y.size))
+
+
+def repack_bytes(n: int, k: int) -> int:
+    return int(lib().q4o_repack_bytes(n, k))
+
+
+def repack(W: np.ndarray, n: int, k: int) -> np.ndarray:
+    """GGUF Q4_0 rows -> the repacked 16 x 256 tile layout (uint8, flat)."""
+    W = _blocks(W, n, k)
+    R = np.empty(repack_bytes(n, k), np.uint8)
+    if R.size == 0 or lib().q4o_repack(_ptr(W, ctypes.c_uint8), n, k,
+                                       _ptr(R, ctypes.c_uint8)) != OK:
+        raise ValueError("q4o_repack: invalid arguments")
+    return R
+
+
+def unrepack(R: np.ndarray, n: int, k: int) -> np.ndarray:
+    R = np.ascontiguousarray(R, dtype=np.uint8).ravel()
+    if R.size != repack_bytes(n, k):
+        raise ValueError("repacked size does not match")
+    W = np.empty((n, k // BLOCK_ELEMS * BLOCK_BYTES), np.uint8)
+    if lib().q4o_unrepack(_ptr(R, ctypes.c_uint8), n, k, _ptr(W, ctypes.c_uint8)) != OK:
+        raise ValueError("q4o_unrepack: invalid arguments")
+    return W
 
 
 def embed_gather(table: np.ndarray, vocab: int, k: int, ids) -> tuple[np.ndarray, int]:

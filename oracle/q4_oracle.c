@@ -229,6 +229,121 @@ int q4o_matmul(const uint8_t* W, int64_t n, int64_t k, const float* X, int64_t m
   return rc;
 }
 
+/* fp64 inputs: the same sum, with x taken as given (no fp32 rounding). */
+int q4o_matmul_f64(const uint8_t* W, int64_t n, int64_t k, const double* X, int64_t m,
+                   int64_t ldx, double* Y, double* S, int64_t ldy, int nthreads) {
+  (void)nthreads;
+  if (!W || !X || !Y || n < 0 || m < 0 || k <= 0 || k % 32 || ldx < k || ldy < n)
+    return Q4O_ERR_INVALID_ARG;
+  int64_t nb = k / 32;
+  float* wrow = (float*)malloc((size_t)k * sizeof(float));
+  if (!wrow) return Q4O_ERR_INVALID_ARG;
+  for (int64_t i = 0; i < n; ++i) {
+    for (int64_t b = 0; b < nb; ++b) q4o_decode_block(W + (i * nb + b) * 18, wrow + b * 32);
+    for (int64_t mm = 0; mm < m; ++mm) {
+      const double* x = X + mm * ldx;
+      double y = 0.0, s = 0.0;
+      for (int64_t kk = 0; kk < k; ++kk) {
+        double p = (double)wrow[kk] * x[kk];
+        y += p;
+        s += fabs(p);
+      }
+      Y[mm * ldy + i] = y;
+      if (S) S[mm * ldy + i] = s;
+    }
+  }
+  free(wrow);
+  return Q4O_OK;
+}
+
+/* ---------------------------------------------------------------- decoder glue */
+
+/* READING (no activation on the pages): SiLU-gated unit, fp64. */
+void q4o_swiglu(const double* a, const double* b, int64_t n, double* out) {
+  for (int64_t i = 0; i < n; ++i) {
+    double sig = 1.0 / (1.0 + exp(-a[i]));
+    out[i] = a[i] * sig * b[i];
+  }
+}
+
+/* READING: greedy decoding takes the largest logit; among equal maxima the
+ * lowest index; NaN logits never win. */
+int64_t q4o_argmax(const double* y, int64_t n) {
+  int64_t best = -1;
+  for (int64_t i = 0; i < n; ++i) {
+    if (isnan(y[i])) continue;
+    if (best < 0 || y[i] > y[best]) best = i;
+  }
+  return best;
+}
+
+/* ---------------------------------------------------------------- repacked layout */
+
+int64_t q4o_repack_bytes(int64_t n, int64_t k) {
+  if (n <= 0 || k <= 0 || k % 256) return 0;
+  int64_t groups = (n + 15) / 16;
+  return groups * (k / 256) * 2304;
+}
+
+/* Byte offsets of block (row r, block kb) inside the repacked matrix. */
+static void q4o_tile_offsets(int64_t r, int64_t kb, int64_t k, int64_t* scale_off,
+                             int64_t* code_off) {
+  int64_t g = r / 16, t = kb / 8;
+  int64_t h = (r % 16) / 4, j = r % 4, b = kb % 8;
+  int64_t lane = 8 * h + b;
+  int64_t tile = (g * (k / 256) + t) * 2304;
+  *scale_off = tile + 8 * lane + 2 * j;
+  *code_off = tile + 256 + 512 * j + 16 * lane;
+}
+
+int q4o_repack(const uint8_t* W, int64_t n, int64_t k, uint8_t* R) {
+  if (!W || !R || n <= 0 || k <= 0 || k % 256) return Q4O_ERR_INVALID_ARG;
+  int64_t nb = k / 32, groups = (n + 15) / 16;
+  for (int64_t r = 0; r < groups * 16; ++r) {
+    for (int64_t kb = 0; kb < nb; ++kb) {
+      int64_t so, co;
+      q4o_tile_offsets(r, kb, k, &so, &co);
+      if (r >= n) { /* padding row: d = +0, every code 8 */
+        R[so] = 0;
+        R[so + 1] = 0;
+        memset(R + co, 0x88, 16);
+        continue;
+      }
+      const uint8_t* blk = W + (r * nb + kb) * 18;
+      uint8_t q[32];
+      for (int c = 0; c < 16; ++c) {
+        q[c] = blk[2 + c] & 0x0F;
+        q[c + 16] = (blk[2 + c] >> 4) & 0x0F;
+      }
+      R[so] = blk[0];
+      R[so + 1] = blk[1];
+      for (int c = 0; c < 16; ++c) R[co + c] = (uint8_t)(q[2 * c] | (q[2 * c + 1] << 4));
+    }
+  }
+  return Q4O_OK;
+}
+
+int q4o_unrepack(const uint8_t* R, int64_t n, int64_t k, uint8_t* W) {
+  if (!W || !R || n <= 0 || k <= 0 || k % 256) return Q4O_ERR_INVALID_ARG;
+  int64_t nb = k / 32;
+  for (int64_t r = 0; r < n; ++r) {
+    for (int64_t kb = 0; kb < nb; ++kb) {
+      int64_t so, co;
+      q4o_tile_offsets(r, kb, k, &so, &co);
+      uint8_t* blk = W + (r * nb + kb) * 18;
+      uint8_t q[32];
+      for (int c = 0; c < 16; ++c) {
+        q[2 * c] = R[co + c] & 0x0F;
+        q[2 * c + 1] = (R[co + c] >> 4) & 0x0F;
+      }
+      blk[0] = R[so];
+      blk[1] = R[so + 1];
+      for (int c = 0; c < 16; ++c) blk[2 + c] = (uint8_t)(q[c] | (q[c + 16] << 4));
+    }
+  }
+  return Q4O_OK;
+}
+
 /* ---------------------------------------------------------------- gather */
 
 /* READING: the pages look rows up on the CPU; the lookup itself is "row id ->

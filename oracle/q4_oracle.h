@@ -72,6 +72,41 @@ int q4o_matmul(const uint8_t* W, int64_t n, int64_t k, const float* X, int64_t m
 int q4o_embed_gather(const uint8_t* table, int64_t vocab, int64_t k, const int32_t* ids,
                      int64_t n_ids, float* out);
 
+/* Y = W^ X as q4o_matmul, with X given in fp64 (an input that is itself the
+ * exact result of an earlier fp64 step, e.g. the gated FFN activation). */
+int q4o_matmul_f64(const uint8_t* W, int64_t n, int64_t k, const double* X, int64_t m,
+                   int64_t ldx, double* Y, double* S, int64_t ldy, int nthreads);
+
+/* Gated FFN activation between the decoder's w1/w3 and w2 linears.  READING:
+ * the pages name the decoder (GeekNews "Arquitectura") but no activation; the
+ * plainest reading for this Mistral-family decoder is the SiLU-gated unit:
+ *   out[i] = a[i] * sigmoid(a[i]) * b[i],  sigmoid(t) = 1 / (1 + exp(-t)),
+ * in fp64, a = the w1 rows' output, b = the w3 rows' output. */
+void q4o_swiglu(const double* a, const double* b, int64_t n, double* out);
+
+/* Index of the largest y[i] (the greedy next token over the output head's
+ * logits); the lowest index among equal maxima; NaN entries are ignored.
+ * Returns -1 when n <= 0 or every entry is NaN. */
+int64_t q4o_argmax(const double* y, int64_t n);
+
+/* Repacked tile layout of a Q4_0 matrix (this library's GPU-native layout;
+ * the pages name only the GGUF format).  Definition, for k % 256 == 0:
+ *   rows are taken in groups of 16 (the last group padded with rows whose
+ *   blocks have d = +0 and every code 8), k in slices of 256 (8 blocks);
+ *   tile (g, t) = rows 16g..16g+15 x blocks 8t..8t+7 is 2304 bytes at offset
+ *   (g * (k/256) + t) * 2304;
+ *   inside a tile, lane L = 8h + b (h = 0..3, b = 0..7) stands for rows
+ *   16g + 4h + j (j = 0..3) of block 8t + b:
+ *     bytes [8L + 2j, 8L + 2j + 2): that block's binary16 d, little-endian;
+ *     bytes [256 + 512j + 16L, +16): its codes, byte c holding element 2c in
+ *     the low nibble and element 2c + 1 in the high nibble.
+ * q4o_repack_bytes gives the size; q4o_repack / q4o_unrepack convert (the
+ * padding rows are dropped by q4o_unrepack).  Return Q4O_OK or
+ * Q4O_ERR_INVALID_ARG. */
+int64_t q4o_repack_bytes(int64_t n, int64_t k);
+int q4o_repack(const uint8_t* W, int64_t n, int64_t k, uint8_t* R);
+int q4o_unrepack(const uint8_t* R, int64_t n, int64_t k, uint8_t* W);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,5 +1,6 @@
 """Plants plausible mistakes in a temporary copy of the CPU oracle and checks that
-the oracle's pins (tests/test_oracle_pins.py) fail for each one.  The repository's
+the oracle's pins (tests/test_oracle_pins.py, tests/test_oracle_pins_glue.py)
+fail for each one.  The repository's
 oracle is never modified; each mutant is compiled and tested in a temp folder."""
 import os
 import shutil
@@ -25,6 +26,23 @@ MUTANTS = {
     "no_clamp_15": ("if (fq > 15.0f) fq = 15.0f;", "if (fq > 16.0f) fq = 15.0f;"),
     "fp32_accumulate": ("double y = 0.0, s = 0.0;", "float y = 0.0, s = 0.0;"),
     "gather_no_status": ("rc = Q4O_ERR_ID_OUT_OF_RANGE;", "rc = Q4O_OK;"),
+    # decoder glue and the repacked layout
+    "sigmoid_sign": ("double sig = 1.0 / (1.0 + exp(-a[i]));",
+                     "double sig = 1.0 / (1.0 + exp(a[i]));"),
+    "gate_on_up": ("double sig = 1.0 / (1.0 + exp(-a[i]));",
+                   "double sig = 1.0 / (1.0 + exp(-b[i]));"),
+    "no_gate_input": ("out[i] = a[i] * sig * b[i];", "out[i] = sig * b[i];"),
+    "argmax_last_tie": ("if (best < 0 || y[i] > y[best]) best = i;",
+                        "if (best < 0 || y[i] >= y[best]) best = i;"),
+    "argmax_keeps_nan": ("if (isnan(y[i])) continue;", "if (0) continue;"),
+    "repack_lane_order": ("int64_t lane = 8 * h + b;", "int64_t lane = 4 * b + h;"),
+    "repack_gguf_nibbles": ("R[co + c] = (uint8_t)(q[2 * c] | (q[2 * c + 1] << 4));",
+                            "R[co + c] = (uint8_t)(q[c] | (q[c + 16] << 4));"),
+    "repack_scale_slot": ("*scale_off = tile + 8 * lane + 2 * j;",
+                          "*scale_off = tile + 2 * lane + 64 * j;"),
+    "repack_pad_code": ("memset(R + co, 0x88, 16);", "memset(R + co, 0x00, 16);"),
+    "f64_rounds_x": ("double p = (double)wrow[kk] * x[kk];",
+                     "double p = (double)wrow[kk] * (double)(float)x[kk];"),
 }
 
 
@@ -38,6 +56,6 @@ def test_pins_catch_planted_mistake(tmp_path, name):
                         ignore=shutil.ignore_patterns("*.so", "__pycache__", "*.tmp*"))
     (tmp_path / "oracle" / "q4_oracle.c").write_text(src.replace(before, after))
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
-                        "tests/test_oracle_pins.py"], cwd=tmp_path, capture_output=True,
-                       text=True, timeout=600)
+                        "tests/test_oracle_pins.py", "tests/test_oracle_pins_glue.py"],
+                       cwd=tmp_path, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"mutant {name} passed every pin:\n{r.stdout[-2000:]}"
