@@ -317,7 +317,11 @@ int q4o_repack(const uint8_t* W, int64_t n, int64_t k, uint8_t* R) {
       }
       R[so] = blk[0];
       R[so + 1] = blk[1];
-      for (int c = 0; c < 16; ++c) R[co + c] = (uint8_t)(q[2 * c] | (q[2 * c + 1] << 4));
+      for (int c = 0; c < 16; ++c) {
+        int u = c / 4, i = c % 4;
+        int e = 16 * (u / 2) + 4 * i + (u % 2); /* low nibble; high nibble: e + 2 */
+        R[co + c] = (uint8_t)(q[e] | (q[e + 2] << 4));
+      }
     }
   }
   return Q4O_OK;
@@ -333,8 +337,10 @@ int q4o_unrepack(const uint8_t* R, int64_t n, int64_t k, uint8_t* W) {
       uint8_t* blk = W + (r * nb + kb) * 18;
       uint8_t q[32];
       for (int c = 0; c < 16; ++c) {
-        q[2 * c] = R[co + c] & 0x0F;
-        q[2 * c + 1] = (R[co + c] >> 4) & 0x0F;
+        int u = c / 4, i = c % 4;
+        int e = 16 * (u / 2) + 4 * i + (u % 2);
+        q[e] = R[co + c] & 0x0F;
+        q[e + 2] = (R[co + c] >> 4) & 0x0F;
       }
       blk[0] = R[so];
       blk[1] = R[so + 1];

@@ -98,8 +98,11 @@ int64_t q4o_argmax(const double* y, int64_t n);
  *   inside a tile, lane L = 8h + b (h = 0..3, b = 0..7) stands for rows
  *   16g + 4h + j (j = 0..3) of block 8t + b:
  *     bytes [8L + 2j, 8L + 2j + 2): that block's binary16 d, little-endian;
- *     bytes [256 + 512j + 16L, +16): its codes, byte c holding element 2c in
- *     the low nibble and element 2c + 1 in the high nibble.
+ *     bytes [256 + 512j + 16L, +16): its codes as four little-endian 32-bit
+ *     words; nibble m (bits 4m..4m+3) of word u holds element
+ *     16 (u / 2) + 2m + (u % 2), i.e. byte c = 4u + i holds element
+ *     16 (u / 2) + 4i + (u % 2) in its low nibble and that element + 2 in its
+ *     high nibble.
  * q4o_repack_bytes gives the size; q4o_repack / q4o_unrepack convert (the
  * padding rows are dropped by q4o_unrepack).  Return Q4O_OK or
  * Q4O_ERR_INVALID_ARG. */

@@ -36,8 +36,10 @@ MUTANTS = {
                         "if (best < 0 || y[i] >= y[best]) best = i;"),
     "argmax_keeps_nan": ("if (isnan(y[i])) continue;", "if (0) continue;"),
     "repack_lane_order": ("int64_t lane = 8 * h + b;", "int64_t lane = 4 * b + h;"),
-    "repack_gguf_nibbles": ("R[co + c] = (uint8_t)(q[2 * c] | (q[2 * c + 1] << 4));",
+    "repack_gguf_nibbles": ("R[co + c] = (uint8_t)(q[e] | (q[e + 2] << 4));",
                             "R[co + c] = (uint8_t)(q[c] | (q[c + 16] << 4));"),
+    "repack_pair_order": ("int e = 16 * (u / 2) + 4 * i + (u % 2); /* low nibble; high nibble: e + 2 */",
+                          "int e = 16 * (u / 2) + 4 * i + (u % 2) * 2; /* low nibble; high nibble: e + 2 */"),
     "repack_scale_slot": ("*scale_off = tile + 8 * lane + 2 * j;",
                           "*scale_off = tile + 2 * lane + 64 * j;"),
     "repack_pad_code": ("memset(R + co, 0x88, 16);", "memset(R + co, 0x00, 16);"),
