@@ -309,9 +309,13 @@ def _run_stack(args, world, dev, stream, hbm, peak_src, torch):
     inputs = [synth.torch_activations(1, 3072, seed=synth.activation_seed(2000, s), device=dev)
               for s in range(G)]
 
-    def timed(chain):
-        g_multi = dec.capture(inputs, stream, chain=chain)
-        g_one = dec.capture(inputs[:1], stream, chain=chain)
+    def timed(kind):
+        if kind == "fused":
+            g_multi = dec.capture_fused(inputs, stream)
+            g_one = dec.capture_fused(inputs[:1], stream)
+        else:
+            g_multi = dec.capture(inputs, stream, chain=kind == "chain")
+            g_one = dec.capture(inputs[:1], stream, chain=kind == "chain")
 
         def plan(steps):
             return [(g_multi, steps // G), (g_one, steps % G)]
@@ -323,15 +327,18 @@ def _run_stack(args, world, dev, stream, hbm, peak_src, torch):
         torch.cuda.synchronize()
         est = _time_graph_replays(plan(args.steps), stream, torch)
         regions = _region_count(est, world, torch)
-        return _timed_regions(lambda: _time_graph_replays(plan(args.steps), stream, torch),
-                              regions, world, dev, torch)
+        res = _timed_regions(lambda: _time_graph_replays(plan(args.steps), stream, torch),
+                             regions, world, dev, torch)
+        del g_multi, g_one
+        return res
 
-    (ms_chain, reg_chain), clocks_chain = timed(chain=True)
-    (ms_pl, reg_pl), clocks_pl = timed(chain=False)
-    # headline: the faster of the two ways of running the same step
-    use_chain = ms_chain < ms_pl
-    ms, clocks, reg = ((ms_chain, clocks_chain, reg_chain) if use_chain else
-                       (ms_pl, clocks_pl, reg_pl))
+    paths = {}
+    for kind in ("fused", "chain", "per_launch"):
+        (ms_k, reg_k), clk_k = timed(kind)
+        paths[kind] = (ms_k, reg_k, clk_k)
+    # headline: the fastest way of running a step
+    best = min(paths, key=lambda k: paths[k][0])
+    ms, reg, clocks = paths[best]
     ms_step = ms / args.steps
     value = world * wbytes * args.steps / (ms * 1e-3) / 1e9
     achieved = (wbytes + abytes) / (ms_step * 1e-3) / 1e9
@@ -342,12 +349,15 @@ def _run_stack(args, world, dev, stream, hbm, peak_src, torch):
     x_host.copy_(torch.randn((rows, 3072), generator=torch.Generator().manual_seed(7)))
     y_host = torch.empty((rows, 3072), dtype=torch.float32).pin_memory()
     x_dev = torch.empty((1, 3072), dtype=torch.float32, device=dev)
-    g_e2e = dec.capture([x_dev], stream, chain=use_chain)
+    if best == "fused":
+        g_e2e, y_dev = dec.capture_fused([x_dev], stream), dec.x_fused
+    else:
+        g_e2e, y_dev = dec.capture([x_dev], stream, chain=best == "chain"), dec.x
     with torch.cuda.stream(stream):
         for s in range(3):
             x_dev.copy_(x_host[s:s + 1], non_blocking=True)
             g_e2e.replay()
-            y_host[s:s + 1].copy_(dec.x, non_blocking=True)
+            y_host[s:s + 1].copy_(y_dev, non_blocking=True)
     stream.synchronize()
 
     def e2e_region():
@@ -357,7 +367,7 @@ def _run_stack(args, world, dev, stream, hbm, peak_src, torch):
             for s in range(args.steps):
                 x_dev.copy_(x_host[s:s + 1], non_blocking=True)
                 g_e2e.replay()
-                y_host[s:s + 1].copy_(dec.x, non_blocking=True)
+                y_host[s:s + 1].copy_(y_dev, non_blocking=True)
         stream.synchronize()
         return (time.perf_counter() - t0) * 1e3
 
@@ -379,27 +389,25 @@ def _run_stack(args, world, dev, stream, hbm, peak_src, torch):
                               f"(min {reg['min_ms'] / args.steps:.4f}, max "
                               f"{reg['max_ms'] / args.steps:.4f} ms/step), each bracketed by a "
                               f"barrier and synchronize; every graph replayed before timing"),
-                   "graph": (f"CUDA graphs of {G} steps, " +
-                             ("one q4_gemv_chain launch per step" if use_chain else
-                              "104 q4_gemv launches per step with programmatic dependent launch")),
+                   "graph": f"CUDA graphs of {G} steps, {PATH_NOTES[best]}",
+                   "step_function": STEP_FUNCTION[best],
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": args.traffic,
-                     "kernel": "gemv_chain_kernel" if use_chain else "gemv_b1_kernel",
+                     "kernel": KERNELS[best],
                      "peak_source": f"{peak_src} HBM copy bandwidth",
-                     "per_launch": ("algorithmic bytes of one step (one launch) / its time"
-                                    if use_chain else
-                                    "algorithmic bytes of the 104 launches of a step / step time "
-                                    "(every launch of the step is this kernel)")},
-        "step_paths": {
-            "per_launch": {"ms_per_step": ms_pl / args.steps,
-                           "gbs": world * wbytes * args.steps / (ms_pl * 1e-3) / 1e9,
-                           "note": "104 q4_gemv launches (PDL) per step, CUDA graphs"},
-            "chain": {"ms_per_step": ms_chain / args.steps,
-                      "gbs": world * wbytes * args.steps / (ms_chain * 1e-3) / 1e9,
-                      "note": "one q4_gemv_chain launch per step, CUDA graphs"}},
+                     "per_launch": ("algorithmic bytes of the 104 launches of a step / step time "
+                                    "(every launch of the step is this kernel)"
+                                    if best == "per_launch" else
+                                    "algorithmic bytes of one step (one launch) / its time")},
+        "step_paths": {k: {"ms_per_step": v[0] / args.steps,
+                           "gbs": world * wbytes * args.steps / (v[0] * 1e-3) / 1e9,
+                           "frac_of_hbm": wbytes * args.steps / (v[0] * 1e-3) / 1e9 / hbm,
+                           "regions": v[1]["regions"], "note": PATH_NOTES[k],
+                           "step_function": STEP_FUNCTION[k]}
+                       for k, v in paths.items()},
         "e2e": e2e,
-        "gpu_launches": args.steps * (1 if use_chain else dec.launches_per_step()),
+        "gpu_launches": args.steps * (dec.launches_per_step() if best == "per_launch" else 1),
         "clocks": clocks,
     }
 
@@ -423,15 +431,24 @@ def _run_single_gemv(args, dev, stream, hbm, torch):
     out = {"workload": "single Q4_0 GEMV 4096x3072, batch 1, fp32 x and y",
            "algorithmic_bytes_per_call": algo,
            "l2": f"{copies} weight copies rotated ({copies * n * k // 32 * 18 / 1e6:.0f} MB)"}
-    for name, flags in (("q4_gemv_pdl", FLAG_PDL), ("q4_gemv", 0)):
+    from bit_weight_quantized_03_b300 import q4_gemv_r, q4_repack
+    Rs = [q4_repack(W, n, k) for W in Ws]
+    wsr = Workspace(dev)
+    calls = {
+        "q4_gemv_pdl": lambda i: q4_gemv(Ws[i % copies], n, k, x, y=y, workspace=ws,
+                                         flags=FLAG_PDL, stream=stream),
+        "q4_gemv": lambda i: q4_gemv(Ws[i % copies], n, k, x, y=y, workspace=ws, stream=stream),
+        "q4_gemv_r": lambda i: q4_gemv_r(Rs[i % copies], n, k, x, y=y, workspace=wsr,
+                                         stream=stream),
+    }
+    for name, call in calls.items():
         with torch.cuda.stream(stream):
-            q4_gemv(Ws[0], n, k, x, y=y, workspace=ws, stream=stream)
+            call(0)
             stream.synchronize()
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
                 for i in range(reps):
-                    q4_gemv(Ws[i % copies], n, k, x, y=y, workspace=ws, flags=flags,
-                            stream=stream)
+                    call(i)
         _time_graph_replays([(g, 2)], stream, torch)
         us = statistics.median(_time_graph_replays([(g, 1)], stream, torch) for _ in range(7)) \
             / reps * 1e3
@@ -441,6 +458,19 @@ def _run_single_gemv(args, dev, stream, hbm, torch):
     best = min((v["us_per_call"], key) for key, v in out.items() if isinstance(v, dict))
     out["best"] = best[1]
     return out
+
+
+PATH_NOTES = {
+    "fused": "one q4_chain launch per step on the repacked weights",
+    "chain": "one q4_gemv_chain launch per step on the GGUF weights",
+    "per_launch": "104 q4_gemv launches per step with programmatic dependent launch",
+}
+STEP_FUNCTION = {
+    "fused": "per layer: qkv = Wqkv x; h = x + Wo q; g = W1h sigmoid(W1h) W3h; x' = h + W2 g",
+    "chain": "per layer: qkv = Wqkv x; o = Wo q; g = W13 o; x' = W2 g1",
+    "per_launch": "per layer: qkv = Wqkv x; o = Wo q; g = W13 o; x' = W2 g1",
+}
+KERNELS = {"fused": "chain_kernel", "chain": "gemv_chain_kernel", "per_launch": "gemv_b1_kernel"}
 
 
 def _run_head_gather(args, dev, stream, hbm, torch):
@@ -477,6 +507,36 @@ def _run_head_gather(args, dev, stream, hbm, torch):
                               "weight_gbs": head_bytes / (hms * 1e-3) / 1e9,
                               "frac_of_hbm": head_bytes / (hms * 1e-3) / 1e9 / hbm,
                               "note": "226 MB table > L2; consecutive calls re-read it"}
+        del gh
+        # the same head on the repacked table: the product, and the argmax of
+        # the logits without writing them (one q4_chain link)
+        from bit_weight_quantized_03_b300 import (OP_ARGMAX, Link, q4_chain, q4_gemv_r,
+                                                  q4_repack)
+        Rt = q4_repack(table, V, H)
+        wsr = Workspace(dev)
+        am = torch.zeros(2, dtype=torch.int32, device=dev)
+        variants = {
+            "q4_gemv_r": lambda: q4_gemv_r(Rt, V, H, xh, y=logits, workspace=wsr, stream=stream),
+            "argmax_no_logits": lambda: q4_chain([Link(Rt, V, H, xh, argmax=am, ops=OP_ARGMAX)],
+                                                 workspace=wsr, stream=stream),
+        }
+        for name, call in variants.items():
+            with torch.cuda.stream(stream):
+                call()
+                stream.synchronize()
+                gv = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gv, stream=stream):
+                    for _ in range(reps):
+                        call()
+            _time_graph_replays([(gv, 2)], stream, torch)
+            vms = statistics.median(_time_graph_replays([(gv, 1)], stream, torch)
+                                    for _ in range(5)) / reps
+            algo = head_bytes + 4 * H + (4 * V if name == "q4_gemv_r" else 8)
+            extra["head_gemv"][name] = {"us_per_call": vms * 1e3,
+                                        "weight_gbs": head_bytes / (vms * 1e-3) / 1e9,
+                                        "frac_of_hbm": algo / (vms * 1e-3) / 1e9 / hbm}
+            del gv
+        del Rt
         gather = {}
         for B in (1, 64, 4096):
             ids = synth.torch_token_ids(B, V, seed=B, device=dev)
@@ -494,7 +554,7 @@ def _run_head_gather(args, dev, stream, hbm, torch):
             nbytes = B * (H // 32 * 18 + H * 4 + 4)
             gather[str(B)] = {"us_per_call": gms * 1e3, "gbs": nbytes / (gms * 1e-3) / 1e9}
         extra["embed_gather"] = gather
-        del table, gh
+        del table
     return extra
 
 

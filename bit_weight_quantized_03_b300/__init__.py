@@ -14,16 +14,19 @@ per token).
 """
 from __future__ import annotations
 
-from ._lib import (BF16, BLOCK_BYTES, CHAIN_MAX_STAGES, GemvStage, BLOCK_ELEMS, ERR_CUDA, ERR_ID_OUT_OF_RANGE,  # noqa: F401
+from ._lib import (BF16, BLOCK_BYTES, CHAIN_MAX_LINKS, CHAIN_MAX_STAGES, GemvStage,  # noqa: F401
+                   BLOCK_ELEMS, ChainLink, ChainSrc, ERR_CUDA, ERR_ID_OUT_OF_RANGE,
                    ERR_INVALID_ARG, ERR_MISALIGNED, ERR_NONFINITE, ERR_TIMEOUT,
                    ERR_UNSUPPORTED_SHAPE, ERR_WORKSPACE, F32, FLAG_PDL, FLAG_TEST_STALL,
-                   GEMV_MAX_M, GEMV_NOALLOC_SCRATCH_BYTES, OK, Q4Error, check, lib,
-                   status_string)
+                   GEMV_MAX_M, GEMV_NOALLOC_SCRATCH_BYTES, OK, OP_ARGMAX, OP_RESIDUAL,
+                   OP_SWIGLU, Q4Error, REPACK_TILE_BYTES, check, lib, status_string)
 
 __all__ = [
     "q4_quantize", "q4_dequant_rows", "q4_gemv", "q4_gemv_noalloc", "q4_gemv_chain", "q4_gemm", "q4_embed_gather", "q4_linear",
     "q4_gemv_workspace_bytes", "q4_gemm_workspace_bytes", "q4_linear_workspace_bytes",
     "q4_linear_crossover_m", "Workspace", "Q4Error", "lib", "packed_bytes",
+    "q4_repack", "q4_repack_bytes", "q4_chain", "q4_chain_workspace_bytes", "q4_gemv_r",
+    "q4_gemv_r_workspace_bytes", "Link", "LinkOut", "interleave_gate_rows",
 ]
 
 
@@ -80,15 +83,20 @@ class Workspace:
 
 
 _default_ws = {}
+# q4_chain / q4_gemv_r carry state in their workspace from call to call (it is
+# not left zero-filled), so they never share the default workspace of the
+# calls that expect an all-zero one.
+_default_chain_ws = {}
 
 
-def _workspace(ws, nbytes: int):
+def _workspace(ws, nbytes: int, chain: bool = False):
     torch = _torch()
     if nbytes <= 0:
         return None, 0
     if ws is None:
         dev = torch.cuda.current_device()
-        ws = _default_ws.setdefault(dev, Workspace(dev))
+        pool = _default_chain_ws if chain else _default_ws
+        ws = pool.setdefault(dev, Workspace(dev))
     if isinstance(ws, Workspace):
         buf = ws.get(nbytes)
     else:
@@ -227,3 +235,102 @@ def q4_linear(W, n: int, k: int, X, Y=None, workspace=None, status=None, flags: 
     check(lib().q4_linear(_ptr(W), n, k, _ptr(X), code, m, ldx, _ptr(Y), ldy, _ptr(buf), nbytes,
                           _ptr(status), flags, _stream(stream)), "q4_linear")
     return Y
+
+
+# ------------------------------------------------------------------ repacked layout, chains
+
+def q4_repack_bytes(n: int, k: int) -> int:
+    return int(lib().q4_repack_bytes(n, k))
+
+
+def q4_repack(W, n: int, k: int, R=None, stream=None):
+    """GGUF Q4_0 [n, k/32*18] -> the repacked tile layout (uint8, flat)."""
+    torch = _torch()
+    if R is None:
+        R = torch.empty(q4_repack_bytes(n, k), dtype=torch.uint8, device=W.device)
+    check(lib().q4_repack(_ptr(W), n, k, _ptr(R), _stream(stream)), "q4_repack")
+    return R
+
+
+class LinkOut:
+    """A chain input taken from an earlier link's output, from element `offset`."""
+
+    def __init__(self, link: int, offset: int = 0):
+        self.link, self.offset = int(link), int(offset)
+
+
+class Link:
+    """One product of a q4_chain: y = W x (+ residual), W repacked (n x k).
+
+    x, residual: a float32 device tensor (read from memory, `*_offset`
+    elements in) or a LinkOut.  ops: OP_SWIGLU | OP_RESIDUAL | OP_ARGMAX
+    (OP_SWIGLU: rows are 8 gate rows then 8 up rows per 16-row group, and the
+    output is their n/2 gated values)."""
+
+    def __init__(self, R, n, k, x, y=None, residual=None, argmax=None, ops=0, x_offset=0,
+                 residual_offset=0):
+        self.R, self.n, self.k, self.y, self.argmax, self.ops = R, n, k, y, argmax, ops
+        self.x, self.residual = x, residual
+        self.offsets = (x_offset, residual_offset)
+
+
+def _src(v, offset):
+    s = ChainSrc()
+    if v is None:
+        s.ptr, s.link, s.offset = None, -1, 0
+    elif isinstance(v, LinkOut):
+        s.ptr, s.link, s.offset = None, v.link, v.offset
+    else:
+        s.ptr, s.link, s.offset = _ptr(v), -1, int(offset)
+    return s
+
+
+def _link_array(links):
+    arr = (ChainLink * len(links))()
+    for i, l in enumerate(links):
+        a = arr[i]
+        a.R, a.n, a.k = _ptr(l.R), l.n, l.k
+        a.x = _src(l.x, l.offsets[0])
+        a.residual = _src(l.residual, l.offsets[1])
+        a.y, a.argmax, a.ops = _ptr(l.y), _ptr(l.argmax), l.ops
+    return arr
+
+
+def q4_chain_workspace_bytes(links) -> int:
+    return int(lib().q4_chain_workspace_bytes(_link_array(links), len(links)))
+
+
+def q4_chain(links, workspace=None, status=None, flags: int = 0, stream=None):
+    """Run the links in one launch (decode-step chain); see q4.h q4_chain."""
+    arr = _link_array(links)
+    need = int(lib().q4_chain_workspace_bytes(arr, len(links)))
+    buf, nbytes = _workspace(workspace, need, chain=True)
+    check(lib().q4_chain(arr, len(links), _ptr(buf), nbytes, _ptr(status), flags,
+                         _stream(stream)), "q4_chain")
+
+
+def q4_gemv_r_workspace_bytes(n: int, k: int) -> int:
+    return int(lib().q4_gemv_r_workspace_bytes(n, k))
+
+
+def q4_gemv_r(R, n: int, k: int, x, y=None, workspace=None, status=None, flags: int = 0,
+              stream=None):
+    """y = W x (batch 1, fp32) on a repacked matrix; x fp32 [k] (or [1, k])."""
+    torch = _torch()
+    if y is None:
+        y = torch.empty((1, n), dtype=torch.float32, device=x.device)
+    buf, nbytes = _workspace(workspace, q4_gemv_r_workspace_bytes(n, k), chain=True)
+    check(lib().q4_gemv_r(_ptr(R), n, k, _ptr(x), _ptr(y), _ptr(buf), nbytes, _ptr(status),
+                          flags, _stream(stream)), "q4_gemv_r")
+    return y
+
+
+def interleave_gate_rows(W1, W3):
+    """Q4_0 rows of the FFN's w1 (gate) and w3 (up), [n, k/32*18] each with
+    n % 8 == 0 -> one [2n, k/32*18] matrix of 16-row groups, 8 w1 rows then
+    the same 8 rows of w3: the row order q4_chain's OP_SWIGLU takes."""
+    torch = _torch()
+    n, rb = W1.shape
+    if W3.shape != W1.shape or n % 8:
+        raise ValueError("w1 and w3 must have the same shape, with rows a multiple of 8")
+    return torch.stack([W1.reshape(n // 8, 8, rb), W3.reshape(n // 8, 8, rb)], dim=1).reshape(2 * n, rb)

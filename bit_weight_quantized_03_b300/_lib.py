@@ -36,6 +36,25 @@ class GemvStage(ctypes.Structure):
 
 
 CHAIN_MAX_STAGES = 128
+CHAIN_MAX_LINKS = 128
+OP_SWIGLU = 1
+OP_RESIDUAL = 2
+OP_ARGMAX = 4
+REPACK_TILE_BYTES = 2304
+
+
+class ChainSrc(ctypes.Structure):
+    """struct q4_chain_src of include/q4.h."""
+    _fields_ = [("ptr", ctypes.c_void_p), ("link", ctypes.c_int32), ("offset", ctypes.c_int32)]
+
+
+class ChainLink(ctypes.Structure):
+    """struct q4_chain_link of include/q4.h."""
+    _fields_ = [("R", ctypes.c_void_p), ("n", ctypes.c_int64), ("k", ctypes.c_int64),
+                ("x", ChainSrc), ("residual", ChainSrc),
+                ("y", ctypes.c_void_p), ("argmax", ctypes.c_void_p), ("ops", ctypes.c_uint32),
+                ("reserved", ctypes.c_uint32)]
+
 
 # Every symbol include/q4.h declares, with its ctypes signature.
 _vp, _i64, _sz, _u32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t, ctypes.c_uint32
@@ -56,6 +75,12 @@ SIGNATURES = {
                         _u32, _vp]),
     "q4_linear_workspace_bytes": (_sz, [_i64, _i64, _i64, ctypes.c_int]),
     "q4_linear_crossover_m": (_i64, [_i64, _i64]),
+    "q4_repack_bytes": (_sz, [_i64, _i64]),
+    "q4_repack": (_st, [_vp, _i64, _i64, _vp, _vp]),
+    "q4_chain_workspace_bytes": (_sz, [ctypes.POINTER(ChainLink), ctypes.c_int32]),
+    "q4_chain": (_st, [ctypes.POINTER(ChainLink), ctypes.c_int32, _vp, _sz, _vp, _u32, _vp]),
+    "q4_gemv_r_workspace_bytes": (_sz, [_i64, _i64]),
+    "q4_gemv_r": (_st, [_vp, _i64, _i64, _vp, _vp, _vp, _sz, _vp, _u32, _vp]),
     "q4_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "q4_version": (ctypes.c_char_p, []),
 }

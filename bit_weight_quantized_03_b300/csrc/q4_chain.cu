@@ -1,0 +1,1058 @@
+// q4_chain.cu -- the repacked Q4_0 layout (q4_repack) and the decode-step
+// chain kernel behind q4_chain / q4_gemv_r.
+//
+// One decode step of the Voxtral Mini 4B Realtime port (GeekNews,
+// es.news.hada.io/topic?id=26595, "Arquitectura": a 26-layer decoder, hidden
+// 3072, GQA 32Q/8KV, GGUF Q4_0 weights) is a chain of batch-1 products, each
+// reading the previous one's output: per layer qkv, wo (+ the residual), the
+// gated FFN pair w1/w3 and w2 (+ the residual), and at the end the output head,
+// whose largest logit is the next token.  Every product streams its weights
+// from HBM once; the products are short (1-5 us of weight traffic each), so
+// what a step costs beyond the weight traffic is the hand-off between
+// products, of which there are 104 per step.
+//
+// Design (one cooperative launch, one 16-warp CTA per SM):
+//   * Weights are read in the repacked 16-row x 256-column tiles (2304 bytes,
+//     q4r_tile.cuh) with one 1-D bulk copy per tile.  Link s's T tiles are cut
+//     into contiguous CTA ranges [T c / C, T (c+1) / C), each CTA range into 16
+//     contiguous warp ranges.  Each warp streams its own tiles through a ring of
+//     four slots and runs ahead into later links while it waits, so the weight
+//     stream does not stop at a hand-off.
+//   * A warp sums its tiles' row products per 16-row group; at the end of a
+//     link the CTA adds its warps' group sums in warp order and publishes one
+//     partial per (group, CTA) into a slot of 16 floats in the workspace.  The
+//     first owner of a group (the CTA holding its first tile) adds the
+//     residual.  A group is split between at most a few CTAs.
+//   * A link's input is read from the slots of the link that produced it: an
+//     element is the sum of its group's partials in CTA order (so the result
+//     does not depend on timing), and the gated FFN unit x * sigmoid(x) * up is
+//     applied while reading.  There is no grid barrier and no flag: a slot word
+//     holds a NaN pattern that arithmetic never produces until its value is
+//     written, and a reader polls the values themselves.  The workspace keeps
+//     two sets of slots used by alternate launches; each launch puts the set
+//     the next launch will use back to that pattern.
+//   * An output with the argmax op is reduced without writing it: each CTA
+//     takes the largest of the rows it finishes, and CTA 0 reduces the CTAs'
+//     records at the end of the launch.
+//   * Every wait is bounded (about a second) and reports Q4_ERR_TIMEOUT.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "../../include/q4.h"
+#include "q4r_tile.cuh"
+
+namespace q4 {
+namespace {
+
+// 8 warps per SM decode as fast as 16 (the decode is throughput-bound) and
+// leave each thread 255 registers, so the gathers keep every load in flight.
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+constexpr int kStages = 8;           // ring slots per warp (a power of two)
+constexpr int kWarpGroups = 16;      // 16-row groups one warp may touch in one link
+constexpr int kCtaGroups = 64;       // groups one CTA may first-own in a link with a residual
+constexpr int kMaxLinks = Q4_CHAIN_MAX_LINKS;
+constexpr int kMaxK = 12288;
+constexpr int kSlotFloats = 16;      // one 16-row group partial
+constexpr uint32_t kEmpty = 0x7FBADBADu;  // NaN pattern that no arithmetic produces
+constexpr int kHeaderBytes = 512;
+// header words (uint32): epoch, finished-CTA counter, abort flag, reset barrier,
+// clean extent of buffer 0 / 1 (floats), each on its own 64-byte line
+constexpr int kHdrEpoch = 0, kHdrFinished = 16, kHdrAbort = 32, kHdrBarrier = 48;
+constexpr int kHdrClean0 = 64, kHdrClean1 = 80;
+
+// floor(n / d) for 32-bit n by a multiply-high and a shift (constants made on
+// the host), then checked exactly.
+struct Div {
+  uint32_t m, s, d;
+};
+
+__device__ __forceinline__ uint32_t divq(uint32_t n, const Div& v) {
+  uint32_t q =
+      static_cast<uint32_t>((static_cast<uint64_t>(__umulhi(v.m, n)) + n) >> v.s);
+  if (static_cast<uint64_t>(q) * v.d > n) --q;
+  else if (static_cast<uint64_t>(q + 1) * v.d <= n) ++q;
+  return q;
+}
+
+struct ChainLink {
+  const uint8_t* R;
+  float* y;
+  int32_t* argmax;
+  const float* ext[2];   // x, residual read from memory (src_link < 0)
+  int32_t src_link[2];   // earlier link whose output is read, or -1
+  int32_t src_off[2];    // first element of the source
+  int32_t n, k, nsb, groups, tiles;
+  int32_t unit;          // tiles per partition unit: nsb (group-aligned) or 1
+  uint32_t ops;
+  uint32_t slot0;        // first slot of this link in a slot set
+  uint32_t rec0;         // first argmax record (2 floats per CTA) in a slot set
+  Div divU;              // division by the number of units (tiles / unit)
+};
+
+struct ChainArgs {
+  ChainLink L[kMaxLinks];
+  int32_t n_links, kmax;
+  float* set[2];         // the two slot sets
+  uint32_t set_floats;   // floats per set this chain uses
+  uint32_t* hdr;
+  int32_t* status;
+  uint32_t flags;
+  Div divC;              // division by the grid size
+};
+
+enum : uint32_t { kOpSwiglu = Q4_OP_SWIGLU, kOpResidual = Q4_OP_RESIDUAL, kOpArgmax = Q4_OP_ARGMAX };
+
+__device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint4 ld_relaxed_v4(const float* p) {
+  uint4 v;
+  asm volatile("ld.relaxed.gpu.global.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_relaxed_u32(uint32_t* p, uint32_t v) {
+  asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_relaxed_f32(float* p, float v) {
+  asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(__float_as_uint(v)) : "memory");
+}
+
+__device__ __forceinline__ bool empty4(const uint4& v) {
+  return v.x == kEmpty || v.y == kEmpty || v.z == kEmpty || v.w == kEmpty;
+}
+__device__ __forceinline__ float4 as_f4(const uint4& v) {
+  return make_float4(__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z),
+                     __uint_as_float(v.w));
+}
+__device__ __forceinline__ void add4(float4& a, const uint4& v) {
+  a.x += __uint_as_float(v.x);
+  a.y += __uint_as_float(v.y);
+  a.z += __uint_as_float(v.z);
+  a.w += __uint_as_float(v.w);
+}
+
+// Per-link data that a CTA reads in its loops, copied from the kernel
+// parameters into shared memory when the launch starts.  A link's work is cut
+// into units of `unit` tiles (a whole 16-row group, or one tile); CTA c holds
+// units [U c / C, U (c+1) / C), i.e. tiles [ca, cb).
+struct SLink {
+  const uint8_t* R;
+  float* slots;        // this link's slots in the launch's slot set
+  int32_t ca, cb;      // this CTA's tiles
+  int32_t nsb, n;
+  int32_t unit, units;
+  Div divU;
+  uint32_t ops;
+};
+
+// CTAs holding the first and last tile of 16-row group g.
+__device__ __forceinline__ void group_owners(const SLink& S, int g, uint32_t C, int& clo,
+                                             int& chi) {
+  if (S.unit == S.nsb) {
+    clo = chi = static_cast<int>(divq(static_cast<uint32_t>(g + 1) * C - 1u, S.divU));
+  } else {
+    clo = static_cast<int>(divq(static_cast<uint32_t>(g * S.nsb + 1) * C - 1u, S.divU));
+    chi = static_cast<int>(divq(static_cast<uint32_t>((g + 1) * S.nsb) * C - 1u, S.divU));
+  }
+}
+
+__device__ __forceinline__ void warp_range(int ca, int cb, int w, int& a, int& b) {
+  a = ca + (cb - ca) * w / kWarps;
+  b = ca + (cb - ca) * (w + 1) / kWarps;
+}
+
+// What a thread carries around for bounded waits.
+struct Ctx {
+  uint32_t c, C;
+  uint64_t t0;         // start of the current bounded wait
+  int* s_abort;        // shared abort flag of the CTA
+  uint32_t* hdr;
+  int32_t* status;
+};
+
+__device__ __noinline__ void fail(Ctx& x) {
+  if (atomicExch(x.s_abort, 1) == 0) {
+    report(x.status, 6 /* Q4_ERR_TIMEOUT */);
+    atomicExch(x.hdr + kHdrAbort, 1u);
+  }
+}
+
+// True while the bounded wait that started at x.t0 may continue.  A poll that
+// found nothing sleeps a little before the next, so that waiting SMs do not
+// crowd the L2 that the SMs still computing stream their weights through.
+__device__ __forceinline__ bool keep_waiting(Ctx& x, int& spins) {
+  __nanosleep(spins < 4 ? 32 : 128);
+  if ((++spins & 15) != 0) return true;
+  if (*reinterpret_cast<volatile int*>(x.s_abort)) return false;
+  if (ld_relaxed_u32(x.hdr + kHdrAbort) != 0u || global_timer_ns() - x.t0 > kWaitLimitNs) {
+    fail(x);
+    return false;
+  }
+  return true;
+}
+
+// One input of a link, as its reader sees it: slots of an earlier link
+// (slots != nullptr) or a vector in memory (ext).  An output element e of a
+// link sits in group e >> shift at position e & (2^shift - 1) of its slot
+// (shift 4; 3 for a gated link, whose slots hold 8 values).
+struct Src {
+  const float* slots;
+  const float* ext;
+  int32_t off;
+  int32_t nsb, unit, shift;
+  Div divU;
+};
+
+// Elements [e, e + 4) of NS sources (NS = 1, or 2 for the gate) for up to W
+// entries (e < 0: unused).  A link-output element is the sum of its group's
+// partials in CTA order; the first two CTAs of every entry of every source
+// are polled in one pass, further ones (links with fewer tiles than SMs) one
+// after another.  false on abort.
+template <int W, int NS>
+__device__ __forceinline__ bool gather(const Src (&S)[NS], Ctx& x, const int (&e)[W],
+                                       float4 (&out)[NS][W]) {
+  const float* q[NS][W];
+  int clo[NS][W], chi[NS][W];
+  uint4 v0[NS][W], v1[NS][W];
+  bool d0[NS][W], d1[NS][W];
+#pragma unroll
+  for (int j = 0; j < NS; ++j) {
+    SLink L;  // only the fields group_owners reads
+    L.nsb = S[j].nsb;
+    L.unit = S[j].unit;
+    L.divU = S[j].divU;
+#pragma unroll
+    for (int m = 0; m < W; ++m) {
+      d0[j][m] = d1[j][m] = true;
+      clo[j][m] = 0;
+      chi[j][m] = -1;
+      q[j][m] = S[j].slots;
+      if (e[m] < 0) continue;
+      if (S[j].slots == nullptr) {
+        out[j][m] = __ldcg(reinterpret_cast<const float4*>(S[j].ext + S[j].off + e[m]));
+        continue;
+      }
+      const int row = S[j].off + e[m], g = row >> S[j].shift;
+      group_owners(L, g, x.C, clo[j][m], chi[j][m]);
+      q[j][m] = S[j].slots + static_cast<size_t>(g + clo[j][m]) * kSlotFloats +
+                (row & ((1 << S[j].shift) - 1));
+      d0[j][m] = false;
+      d1[j][m] = chi[j][m] <= clo[j][m];
+    }
+  }
+  x.t0 = global_timer_ns();
+  int spins = 0;
+  while (true) {
+#pragma unroll
+    for (int j = 0; j < NS; ++j)
+#pragma unroll
+      for (int m = 0; m < W; ++m) {
+        if (!d0[j][m]) v0[j][m] = ld_relaxed_v4(q[j][m]);
+        if (!d1[j][m]) v1[j][m] = ld_relaxed_v4(q[j][m] + kSlotFloats);
+      }
+    bool all = true;
+#pragma unroll
+    for (int j = 0; j < NS; ++j)
+#pragma unroll
+      for (int m = 0; m < W; ++m) {
+        if (!d0[j][m]) d0[j][m] = !empty4(v0[j][m]);
+        if (!d1[j][m]) d1[j][m] = !empty4(v1[j][m]);
+        all = all && d0[j][m] && d1[j][m];
+      }
+    if (all) break;
+    if (!keep_waiting(x, spins)) return false;
+  }
+#pragma unroll
+  for (int j = 0; j < NS; ++j)
+#pragma unroll
+    for (int m = 0; m < W; ++m) {
+      if (e[m] < 0 || S[j].slots == nullptr) continue;
+      float4 s = as_f4(v0[j][m]);
+      if (chi[j][m] > clo[j][m]) add4(s, v1[j][m]);
+      for (int cc = clo[j][m] + 2; cc <= chi[j][m]; ++cc) {
+        const float* p = q[j][m] + static_cast<size_t>(cc - clo[j][m]) * kSlotFloats;
+        uint4 u;
+        x.t0 = global_timer_ns();
+        int sp = 0;
+        while (true) {
+          u = ld_relaxed_v4(p);
+          if (!empty4(u)) break;
+          if (!keep_waiting(x, sp)) return false;
+        }
+        add4(s, u);
+      }
+      out[j][m] = s;
+    }
+  return true;
+}
+
+__device__ __forceinline__ float silu_gate(float a, float b) { return a / (1.0f + __expf(-a)) * b; }
+
+// Stage x of a link into shared memory (padded layout).
+template <int W>
+__device__ __forceinline__ bool stage_x(const Src& a, int k, float* xs, Ctx& x, int tid0,
+                                        int nthr) {
+  const int quads = k / 4;
+  const Src S[1] = {a};
+  for (int q0 = tid0; q0 < quads; q0 += nthr * W) {
+    int e[W];
+#pragma unroll
+    for (int m = 0; m < W; ++m) {
+      const int q = q0 + m * nthr;
+      e[m] = q < quads ? 4 * q : -1;
+    }
+    float4 v[1][W];
+    if (!gather<W, 1>(S, x, e, v)) return false;
+#pragma unroll
+    for (int m = 0; m < W; ++m)
+      if (e[m] >= 0) *reinterpret_cast<float4*>(xs + rt::xpad(e[m])) = v[0][m];
+  }
+  return true;
+}
+
+// Residual rows of the groups this CTA holds the first tile of -> sres[gl][row]
+// (gl = group - g0c); rows past n read as zero.
+__device__ __forceinline__ bool stage_residual(const Src& r, const SLink& S, int g0c, int gcount,
+                                               float (*sres)[kSlotFloats], Ctx& x, int tid0,
+                                               int nthr) {
+  constexpr int W = 4;
+  const int quads = gcount * 4;
+  for (int q0 = tid0; q0 < quads; q0 += nthr * W) {
+    int e[W];
+#pragma unroll
+    for (int m = 0; m < W; ++m) {
+      const int q = q0 + m * nthr;
+      e[m] = -1;
+      if (q < quads) {
+        const int g = g0c + q / 4;
+        const int row = 16 * g + 4 * (q & 3);
+        int clo, chi;
+        group_owners(S, g, x.C, clo, chi);
+        if (clo == static_cast<int>(x.c) && row < S.n) e[m] = row;
+      }
+    }
+    const Src R1[1] = {r};
+    float4 v[1][W];
+    if (!gather<W, 1>(R1, x, e, v)) return false;
+#pragma unroll
+    for (int m = 0; m < W; ++m) {
+      if (e[m] < 0) continue;
+      const int q = q0 + m * nthr;
+      *reinterpret_cast<float4*>(&sres[q / 4][4 * (q & 3)]) = v[0][m];
+    }
+  }
+  return true;
+}
+
+// Argmax candidates: larger value wins, then the lower index; NaN never wins.
+__device__ __forceinline__ void better(float& bv, int& bi, float v, int i) {
+  if (v != v) return;
+  if (bi < 0 || v > bv || (v == bv && i < bi)) {
+    bv = v;
+    bi = i;
+  }
+}
+__device__ __forceinline__ void warp_best(float& bv, int& bi) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    if (oi >= 0) better(bv, bi, ov, oi);
+  }
+}
+
+// A warp's weight stream: its tiles of every link in order, kStages in flight
+// through its ring.  `left` tiles remain in link ps, the next one at psrc.
+struct TileStream {
+  int ps, left, issued, consumed;
+  const uint8_t* psrc;
+};
+
+__device__ __forceinline__ void stream_enter(const SLink* sl, TileStream& ts, int warp) {
+  const SLink& L = sl[ts.ps];
+  int a, b;
+  warp_range(L.ca, L.cb, warp, a, b);
+  ts.left = b - a;
+  ts.psrc = L.R + static_cast<size_t>(a) * rt::kTileBytes;
+}
+
+__device__ __forceinline__ void stream_settle(const SLink* sl, int n_links, TileStream& ts,
+                                              int warp) {
+  while (ts.ps < n_links && ts.left == 0)
+    if (++ts.ps < n_links) stream_enter(sl, ts, warp);
+}
+
+__device__ __forceinline__ void stream_issue(const SLink* sl, int n_links, TileStream& ts,
+                                             int warp, int lane, uint32_t ring, uint32_t bar0,
+                                             uint64_t pol) {
+  if (ts.ps >= n_links) return;
+  if (lane == 0) {
+    const uint32_t slot = static_cast<uint32_t>(ts.issued) & (kStages - 1);
+    mbar_arrive_expect_tx(bar0 + 8 * slot, rt::kTileBytes);
+    bulk_g2s(ring + slot * rt::kTileBytes, ts.psrc, rt::kTileBytes, bar0 + 8 * slot, pol);
+  }
+  ++ts.issued;
+  ts.psrc += rt::kTileBytes;
+  if (--ts.left == 0) stream_settle(sl, n_links, ts, warp);
+}
+
+// This warp's tiles [wa, wb) of the current link: each 16-row group's row
+// products end in Pw[group - first group][row].  Kept out of line so that the
+// decode loop is register-allocated on its own.
+__device__ __forceinline__ bool run_tiles(const SLink* sl, int n_links, TileStream& tsr, Ctx& x,
+                                       int warp, int lane, uint32_t ring, uint32_t bar0,
+                                       uint32_t xs_addr, int wa, int wb, int nsb,
+                                       float (*Pw)[kSlotFloats]) {
+  TileStream ts = tsr;
+  const uint64_t pol = l2_evict_first_policy();
+  const rt::PairConsts pc = rt::make_pair_consts();
+  const int g0w = wa < wb ? wa / nsb : 0;
+  int cur = -1;
+  float yv[4] = {0.f, 0.f, 0.f, 0.f};
+  auto flush = [&](int g) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float v = yv[j];
+      v += __shfl_xor_sync(0xffffffffu, v, 1);
+      v += __shfl_xor_sync(0xffffffffu, v, 2);
+      v += __shfl_xor_sync(0xffffffffu, v, 4);
+      if ((lane & 7) == 0) Pw[g - g0w][4 * (lane >> 3) + j] = v;
+      yv[j] = 0.f;
+    }
+  };
+  bool ok = true;
+  int g = g0w, t = wa - g0w * nsb;
+  for (int i = wa; i < wb; ++i) {
+    const uint32_t slot = static_cast<uint32_t>(ts.consumed) & (kStages - 1);
+    const uint32_t parity = static_cast<uint32_t>(ts.consumed / kStages) & 1u;
+    const bool landed = mbar_wait(bar0 + 8 * slot, parity, x.s_abort);
+    if (!__all_sync(0xffffffffu, landed)) {
+      if (lane == 0) fail(x);
+      ok = false;
+      break;
+    }
+    if (g != cur) {
+      if (cur >= 0) flush(cur);
+      cur = g;
+    }
+    rt::tile_dot(ring + slot * rt::kTileBytes, xs_addr, t, lane, pc, yv);
+    if (++t == nsb) {
+      t = 0;
+      ++g;
+    }
+    __syncwarp();
+    fence_proxy_async_smem();
+    ++ts.consumed;
+    stream_issue(sl, n_links, ts, warp, lane, ring, bar0, pol);
+  }
+  if (ok && cur >= 0) flush(cur);
+  tsr = ts;
+  return ok;
+}
+
+__device__ __forceinline__ Src make_src(const ChainArgs& A, const SLink* sl, int s, int j) {
+  const ChainLink& L = A.L[s];
+  Src r;
+  const int t = L.src_link[j];
+  r.off = L.src_off[j];
+  r.ext = L.ext[j];
+  r.slots = nullptr;
+  r.nsb = 1;
+  r.unit = 1;
+  r.shift = 4;
+  r.divU = Div{0, 0, 1};
+  if (t >= 0) {
+    r.slots = sl[t].slots;
+    r.nsb = sl[t].nsb;
+    r.unit = sl[t].unit;
+    r.shift = (sl[t].ops & kOpSwiglu) ? 3 : 4;
+    r.divU = sl[t].divU;
+  }
+  return r;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constant__ ChainArgs A) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t full_bar[kWarps][kStages];
+  __shared__ __align__(8) uint64_t never_bar;
+  __shared__ __align__(16) float P[kWarps][kWarpGroups][kSlotFloats];
+  __shared__ __align__(16) float sres[kCtaGroups][kSlotFloats];
+  __shared__ __align__(16) SLink s_links[kMaxLinks];
+  __shared__ int s_wa[kWarps], s_wb[kWarps];
+  __shared__ float sown[kSlotFloats];
+  __shared__ float s_bv[kWarps];
+  __shared__ int s_bi[kWarps];
+  __shared__ int s_abort;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  Ctx x;
+  x.c = blockIdx.x;
+  x.C = gridDim.x;
+  x.s_abort = &s_abort;
+  x.hdr = A.hdr;
+  x.status = A.status;
+  const int n_links = A.n_links;
+  float* xs = reinterpret_cast<float*>(smem);
+  const uint32_t xs_addr = smem_u32(smem);
+  const uint32_t xs_bytes = static_cast<uint32_t>((rt::xpad_floats(A.kmax) * 4 + 127) / 128 * 128);
+  const uint32_t ring = xs_addr + xs_bytes + warp * kStages * rt::kTileBytes;
+  const uint32_t bar0 = smem_u32(&full_bar[warp][0]);
+  const uint64_t pol = l2_evict_first_policy();
+
+  // the header's words are loaded together, first, so that their latency
+  // overlaps the set-up below
+  const uint32_t epoch = ld_relaxed_u32(A.hdr + kHdrEpoch);
+  const uint32_t clean0 = ld_relaxed_u32(A.hdr + kHdrClean0);
+  const uint32_t clean1 = ld_relaxed_u32(A.hdr + kHdrClean1);
+  const int set = static_cast<int>(epoch & 1u);
+  if (tid == 0) {
+    s_abort = 0;
+    mbar_init(smem_u32(&never_bar), 1);
+  }
+  if (lane == 0)
+    for (int i = 0; i < kStages; ++i) mbar_init(bar0 + 8 * i, 1);
+  for (int s = tid; s < n_links; s += kThreads) {
+    const ChainLink& L = A.L[s];
+    SLink& S = s_links[s];
+    const uint32_t units = static_cast<uint32_t>(L.tiles / L.unit);
+    S.R = L.R;
+    S.slots = A.set[set] + static_cast<size_t>(L.slot0) * kSlotFloats;
+    S.ca = L.unit * static_cast<int>(divq(units * x.c, A.divC));
+    S.cb = L.unit * static_cast<int>(divq(units * (x.c + 1), A.divC));
+    S.nsb = L.nsb;
+    S.n = L.n;
+    S.unit = L.unit;
+    S.units = static_cast<int>(units);
+    S.divU = L.divU;
+    S.ops = L.ops;
+  }
+  fence_mbarrier_init();
+  __syncthreads();
+  const uint32_t clean_mine = set ? clean1 : clean0;
+
+  // ---- this warp's weight stream: the first kStages tiles go out now
+  TileStream ts;
+  ts.ps = 0;
+  ts.issued = 0;
+  ts.consumed = 0;
+  stream_enter(s_links, ts, warp);
+  stream_settle(s_links, n_links, ts, warp);
+  for (int i = 0; i < kStages; ++i)
+    stream_issue(s_links, n_links, ts, warp, lane, ring, bar0, pol);
+
+  // ---- slot sets: a fresh workspace (or one last used with a smaller chain)
+  // gets both sets reset before anyone publishes; otherwise the set of the
+  // next launch is reset while this one runs.
+  {
+    const bool fresh = epoch == 0u || clean_mine < A.set_floats;
+    const uint32_t total = A.set_floats / 4;  // float4s per set
+    const uint32_t q0 = divq(total * x.c, A.divC), q1 = divq(total * (x.c + 1), A.divC);
+    const uint4 e4 = make_uint4(kEmpty, kEmpty, kEmpty, kEmpty);
+    for (int st = 0; st < 2; ++st) {
+      if (st == set && !fresh) continue;
+      uint4* p = reinterpret_cast<uint4*>(A.set[st]);
+      for (uint32_t i = q0 + tid; i < q1; i += kThreads) p[i] = e4;
+    }
+    if (fresh) {
+      // every CTA's reset of this launch's set lands before anything is published
+      __syncthreads();
+      if (tid == 0) {
+        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(A.hdr + kHdrBarrier) : "memory");
+        x.t0 = global_timer_ns();
+        int sp = 0;
+        while (ld_acquire_u32(A.hdr + kHdrBarrier) < x.C)
+          if (!keep_waiting(x, sp)) break;
+      }
+      __syncthreads();
+    }
+  }
+
+  // Test hook: one bounded wait that nothing ends (thread 0 of CTA 0, which
+  // every launch has), so the call reports Q4_ERR_TIMEOUT.
+  if ((A.flags & kFlagTestStallOneWait) != 0 && x.c == 0 && tid == 0)
+    if (!mbar_wait(smem_u32(&never_bar), 0, &s_abort)) fail(x);
+  float bv = 0.f;  // argmax candidate of this thread
+  int bi = -1;
+  // Every decision taken on the abort flag is made uniform by a barrier that
+  // ORs it over the CTA, so that no warp or CTA splits around a collective.
+  volatile int* abort_flag = &s_abort;
+  bool stop = false;
+
+  for (int s = 0; s <= n_links; ++s) {
+    // ---------------- finish link s-1: the CTA's split first-owned group
+    if (s > 0 && warp == kWarps - 1 && !stop) {
+      const ChainLink& P1 = A.L[s - 1];
+      const SLink& S1 = s_links[s - 1];
+      float fv = 0.f;
+      int fi = -1;
+      if (S1.ca < S1.cb && (P1.y != nullptr || (S1.ops & kOpArgmax))) {
+        const int g = (S1.cb - 1) / S1.nsb;
+        int clo, chi;
+        group_owners(S1, g, x.C, clo, chi);
+        if (clo == static_cast<int>(x.c) && chi > clo && lane < kSlotFloats) {
+          float v = sown[lane];
+          bool ok = true;
+          for (int cc = clo + 1; cc <= chi && ok; ++cc) {
+            const uint32_t* q = reinterpret_cast<const uint32_t*>(
+                S1.slots + static_cast<size_t>(g + cc) * kSlotFloats + lane);
+            x.t0 = global_timer_ns();
+            int sp = 0;
+            uint32_t u;
+            while ((u = ld_relaxed_u32(q)) == kEmpty)
+              if (!keep_waiting(x, sp)) {
+                ok = false;
+                break;
+              }
+            v += __uint_as_float(u);
+          }
+          const int row = 16 * g + lane;
+          if (ok && row < S1.n) {
+            if (P1.y != nullptr) P1.y[row] = v;
+            better(fv, fi, v, row);
+          }
+        }
+      }
+      if (S1.ops & kOpArgmax) {
+        // this CTA's record: its fully held rows (from the publish step) and
+        // the split group finished here, reduced in a fixed order
+        warp_best(fv, fi);
+        if (lane == 0) {
+          float v = fv;
+          int i = fi;
+          for (int w = 0; w < kWarps; ++w)
+            if (s_bi[w] >= 0) better(v, i, s_bv[w], s_bi[w]);
+          float* rec = A.set[set] + P1.rec0 + 2 * x.c;
+          st_relaxed_f32(rec, i >= 0 ? v : 0.f);
+          st_relaxed_f32(rec + 1, __int_as_float(i));
+        }
+      }
+    }
+    if (s == n_links) break;
+    const SLink& S = s_links[s];
+    const int ca = S.ca, cb = S.cb;
+    const int g0c = ca < cb ? ca / S.nsb : 0;
+    const int gcount = ca < cb ? (cb - 1) / S.nsb - g0c + 1 : 0;
+    if (lane == 0) {
+      int a, b;
+      warp_range(ca, cb, warp, a, b);
+      s_wa[warp] = a;
+      s_wb[warp] = b;
+    }
+
+    // ---------------- stage x_s (and the residual rows this CTA adds)
+    if (!*abort_flag && ca < cb) {
+      // every thread keeps up to 9 element quads in flight: one pass for k <= 9216
+      const bool ok = stage_x<9>(make_src(A, s_links, s, 0), A.L[s].k, xs, x, tid, kThreads);
+      if (ok && (S.ops & kOpResidual) && gcount > 0)
+        stage_residual(make_src(A, s_links, s, 1), S, g0c, gcount, sres, x, tid, kThreads);
+    }
+    stop = __syncthreads_or(*abort_flag) != 0;
+    if (stop) break;
+
+    // ---------------- this warp's tiles of link s
+    run_tiles(s_links, n_links, ts, x, warp, lane, ring, bar0, xs_addr, s_wa[warp], s_wb[warp],
+              S.nsb, P[warp]);
+    stop = __syncthreads_or(*abort_flag) != 0;
+    if (stop) break;
+
+    // ---------------- publish: one partial per (group, CTA); y and argmax
+    // candidates for the groups held whole
+    bi = -1;
+    if (ca == cb && tid < kSlotFloats) {
+      // A CTA without tiles in this link sits at tile ca, inside the group
+      // ca / nsb when the link has fewer tiles than SMs; readers of that group
+      // count it among the group's CTAs, so it publishes zeros there.  Its
+      // slot index ca / nsb + c is still unique.
+      st_relaxed_f32(S.slots + static_cast<size_t>(ca / S.nsb + x.c) * kSlotFloats + tid, 0.f);
+    }
+    if (gcount > 0 && (S.ops & kOpSwiglu)) {
+      // gated link (whole groups): 8 values per group, a * sigmoid(a) * b
+      float* const y = A.L[s].y;
+      for (int idx = tid; idx < gcount * 8; idx += kThreads) {
+        const int gl = idx >> 3, j = idx & 7, g = g0c + gl;
+        const int t0 = g * S.nsb, t1 = t0 + S.nsb;
+        float a = 0.f, b = 0.f;
+        for (int w = 0; w < kWarps; ++w) {
+          const int wa = s_wa[w], wb = s_wb[w];
+          if (wa < wb && wa < t1 && wb > t0) {
+            a += P[w][g - wa / S.nsb][j];
+            b += P[w][g - wa / S.nsb][j + 8];
+          }
+        }
+        const float v = silu_gate(a, b);
+        st_relaxed_f32(S.slots + static_cast<size_t>(g + x.c) * kSlotFloats + j, v);
+        if (y != nullptr && 8 * g + j < S.n / 2) y[8 * g + j] = v;
+      }
+    } else if (gcount > 0) {
+      float* const y = A.L[s].y;
+      for (int idx = tid; idx < gcount * kSlotFloats; idx += kThreads) {
+        const int gl = idx >> 4, row16 = idx & 15, g = g0c + gl;
+        const int t0 = g * S.nsb, t1 = t0 + S.nsb;
+        float sum = 0.f;
+        for (int w = 0; w < kWarps; ++w) {
+          const int a = s_wa[w], b = s_wb[w];
+          if (a < b && a < t1 && b > t0) sum += P[w][g - a / S.nsb][row16];
+        }
+        int clo, chi;
+        group_owners(S, g, x.C, clo, chi);
+        const bool first = clo == static_cast<int>(x.c);
+        if (first && (S.ops & kOpResidual)) sum += sres[gl][row16];
+        st_relaxed_f32(S.slots + static_cast<size_t>(g + x.c) * kSlotFloats + row16, sum);
+        const int row = 16 * g + row16;
+        if (first) {
+          if (chi == clo) {
+            if (row < S.n) {
+              if (y != nullptr) y[row] = sum;
+              better(bv, bi, sum, row);
+            }
+          } else {
+            sown[row16] = sum;
+          }
+        }
+      }
+    }
+    if (S.ops & kOpArgmax) {
+      warp_best(bv, bi);
+      if (lane == 0) {
+        s_bv[warp] = bv;
+        s_bi[warp] = bi;
+      }
+    }
+    stop = __syncthreads_or(*abort_flag) != 0;
+    if (stop) break;
+  }
+
+  // ---------------- argmax over the CTAs' records (CTA 0), then the epoch
+  stop = __syncthreads_or(*abort_flag) != 0;
+  if (!stop && x.c == 0 && warp == 0) {
+    for (int s = 0; s < n_links; ++s) {
+      const ChainLink& L = A.L[s];
+      if (!(L.ops & kOpArgmax)) continue;
+      const uint32_t* rec = reinterpret_cast<const uint32_t*>(A.set[set] + L.rec0);
+      float v = 0.f;
+      int i = -1;
+      bool ok = true;
+      for (uint32_t cc = lane; cc < x.C; cc += 32) {
+        x.t0 = global_timer_ns();
+        int sp = 0;
+        uint32_t rv, ri;
+        while (true) {
+          rv = ld_relaxed_u32(rec + 2 * cc);
+          ri = ld_relaxed_u32(rec + 2 * cc + 1);
+          if (rv != kEmpty && ri != kEmpty) break;
+          if (!keep_waiting(x, sp)) {
+            ok = false;
+            break;
+          }
+        }
+        if (!ok) break;
+        if (static_cast<int>(ri) >= 0) better(v, i, __uint_as_float(rv), static_cast<int>(ri));
+      }
+      warp_best(v, i);
+      const bool all_ok = __all_sync(0xffffffffu, ok);  // every lane votes
+      if (lane == 0 && all_ok) {
+        L.argmax[0] = i;
+        L.argmax[1] = __float_as_int(i >= 0 ? v : __uint_as_float(0x7FC00000u));
+      }
+    }
+  }
+  __syncthreads();
+  if (tid == 0 && !*abort_flag) {
+    // the last CTA to finish records that the next set is clean and moves the epoch
+    const uint32_t prev = atomicAdd(A.hdr + kHdrFinished, 1u);
+    if (prev == x.C - 1) {
+      // every other CTA is done with the header: plain stores, nothing waits
+      st_relaxed_u32(A.hdr + kHdrFinished, 0u);
+      st_relaxed_u32(A.hdr + kHdrBarrier, 0u);
+      st_relaxed_u32(A.hdr + (set ? kHdrClean0 : kHdrClean1), A.set_floats);
+      st_relaxed_u32(A.hdr + kHdrEpoch, epoch + 1u);
+    }
+  }
+  // copies this warp still has in flight land before the CTA exits
+  for (int q = ts.consumed; q < ts.issued; ++q)
+    mbar_wait(bar0 + 8 * static_cast<uint32_t>(q % kStages),
+              static_cast<uint32_t>((q / kStages) & 1));
+}
+
+// ------------------------------------------------------------------ repack
+// Thread per (row, block) of the padded matrix: GGUF block -> repacked tile.
+__global__ void __launch_bounds__(256) repack_kernel(const uint8_t* __restrict__ W, int64_t n,
+                                                     int64_t k, uint8_t* __restrict__ R) {
+  const int64_t nb = k / 32, rows = (n + 15) / 16 * 16;
+  const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= rows * nb) return;
+  const int64_t r = idx / nb, kb = idx - r * nb;
+  const int64_t g = r / 16, t = kb / 8;
+  const int h = static_cast<int>((r & 15) >> 2), j = static_cast<int>(r & 3);
+  const int b = static_cast<int>(kb & 7), L = 8 * h + b;
+  uint8_t* tile = R + (g * (k / 256) + t) * rt::kTileBytes;
+  uint32_t dbits = 0;
+  uint32_t q[16];
+  if (r < n) {
+    const uint8_t* blk = W + (r * nb + kb) * kBlockBytes;
+    dbits = blk[0] | (static_cast<uint32_t>(blk[1]) << 8);
+    uint8_t qs[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) qs[c] = blk[2 + c];
+    // GGUF: byte c = element c | element c+16 << 4.  Here byte c = 4u + i
+    // (word u) holds element e = 16 (u / 2) + 4i + (u % 2) low and e + 2 high.
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const int u = c >> 2, i = c & 3;
+      const int e0 = 16 * (u >> 1) + 4 * i + (u & 1), e1 = e0 + 2;
+      const uint32_t q0 = e0 < 16 ? (qs[e0] & 0xF) : (qs[e0 - 16] >> 4);
+      const uint32_t q1 = e1 < 16 ? (qs[e1] & 0xF) : (qs[e1 - 16] >> 4);
+      q[c] = q0 | (q1 << 4);
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < 16; ++c) q[c] = 0x88;
+  }
+  *reinterpret_cast<uint16_t*>(tile + 8 * L + 2 * j) = static_cast<uint16_t>(dbits);
+  uint4 v;
+  v.x = q[0] | (q[1] << 8) | (q[2] << 16) | (q[3] << 24);
+  v.y = q[4] | (q[5] << 8) | (q[6] << 16) | (q[7] << 24);
+  v.z = q[8] | (q[9] << 8) | (q[10] << 16) | (q[11] << 24);
+  v.w = q[12] | (q[13] << 8) | (q[14] << 16) | (q[15] << 24);
+  *reinterpret_cast<uint4*>(tile + rt::kScaleBytes + rt::kCodeRowBytes * j + 16 * L) = v;
+}
+
+// ------------------------------------------------------------------ host side
+Div make_div(uint32_t d) {
+  uint32_t l = 0;
+  while ((uint64_t(1) << l) < d) ++l;
+  const uint64_t m = ((uint64_t(1) << 32) * ((uint64_t(1) << l) - d)) / d + 1;
+  return {static_cast<uint32_t>(m), l, d};
+}
+
+inline bool aligned(const void* p, uintptr_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
+
+}  // namespace
+
+// Validates the links and fills the kernel arguments; returns the workspace
+// bytes the chain needs in *ws.
+q4_status chain_plan(const q4_chain_link* links, int32_t n, ChainArgs* A, size_t* ws) {
+  if (links == nullptr || n < 1 || n > kMaxLinks) return Q4_ERR_INVALID_ARG;
+  const uint32_t C = static_cast<uint32_t>(sm_count());
+  int kmax = 256;
+  uint32_t slot = 0, rec_floats = 0;
+  // argmax records go after every link's slots; first count the slots
+  uint32_t slots_total = 0;
+  for (int32_t s = 0; s < n; ++s) {
+    const q4_chain_link& l = links[s];
+    if (l.n <= 0 || l.k <= 0 || l.n > (int64_t(1) << 28)) return Q4_ERR_INVALID_ARG;
+    const int64_t groups = (l.n + 15) / 16;
+    slots_total += static_cast<uint32_t>(groups + C);
+  }
+  for (int32_t s = 0; s < n; ++s) {
+    const q4_chain_link& l = links[s];
+    if (l.R == nullptr) return Q4_ERR_INVALID_ARG;
+    if (l.k % 256 != 0 || l.k > kMaxK) return Q4_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(l.R, 16)) return Q4_ERR_MISALIGNED;
+    if (l.ops & ~uint32_t(Q4_OP_SWIGLU | Q4_OP_RESIDUAL | Q4_OP_ARGMAX)) return Q4_ERR_INVALID_ARG;
+    if (l.y != nullptr && !aligned(l.y, 4)) return Q4_ERR_MISALIGNED;
+    if ((l.ops & Q4_OP_ARGMAX) && (l.argmax == nullptr || !aligned(l.argmax, 4)))
+      return Q4_ERR_INVALID_ARG;
+    const bool gate = (l.ops & Q4_OP_SWIGLU) != 0;
+    if (gate && (l.ops != Q4_OP_SWIGLU || l.n % 16 != 0)) return Q4_ERR_INVALID_ARG;
+    const int64_t groups = (l.n + 15) / 16, nsb = l.k / 256, tiles = groups * nsb;
+    if (tiles * C >= (int64_t(1) << 31)) return Q4_ERR_UNSUPPORTED_SHAPE;
+    // Work is cut into whole 16-row groups when that costs the busiest CTA at
+    // most 1/16 more tiles than cutting single tiles: a group then has one
+    // owner, whose partial is its final value.
+    const int64_t per_tile = (tiles + C - 1) / C, per_group = (groups + C - 1) / C * nsb;
+    // A gated link is always cut at whole groups: the owner of a group applies
+    // the gate to its 8 row pairs.
+    const int64_t unit = (gate || per_group <= per_tile + per_tile / 16) ? nsb : 1;
+    // bounded shared-memory bookkeeping per warp and per CTA
+    const int64_t per_cta = unit == 1 ? per_tile : per_group;
+    const int64_t per_warp = (per_cta + kWarps - 1) / kWarps;
+    if (per_warp / nsb + 2 > kWarpGroups) return Q4_ERR_UNSUPPORTED_SHAPE;
+    if ((l.ops & Q4_OP_RESIDUAL) && per_cta / nsb + 2 > kCtaGroups) return Q4_ERR_UNSUPPORTED_SHAPE;
+    // sources: x (k elements) and the residual (n elements)
+    const q4_chain_src* src[2] = {&l.x, &l.residual};
+    const bool used[2] = {true, (l.ops & Q4_OP_RESIDUAL) != 0};
+    const int64_t len[2] = {l.k, l.n};
+    if (A != nullptr) {
+      ChainLink& c = A->L[s];
+      c.R = static_cast<const uint8_t*>(l.R);
+      c.y = l.y;
+      c.argmax = l.argmax;
+      c.n = static_cast<int32_t>(l.n);
+      c.k = static_cast<int32_t>(l.k);
+      c.nsb = static_cast<int32_t>(nsb);
+      c.groups = static_cast<int32_t>(groups);
+      c.tiles = static_cast<int32_t>(tiles);
+      c.ops = l.ops;
+      c.slot0 = slot;
+      c.unit = static_cast<int32_t>(unit);
+      c.divU = make_div(static_cast<uint32_t>(tiles / unit));
+      c.rec0 = 0;
+    }
+    for (int j = 0; j < 2; ++j) {
+      if (A != nullptr) {
+        A->L[s].ext[j] = nullptr;
+        A->L[s].src_link[j] = -1;
+        A->L[s].src_off[j] = 0;
+      }
+      if (!used[j]) continue;
+      const q4_chain_src& q = *src[j];
+      if (q.offset < 0) return Q4_ERR_INVALID_ARG;
+      if (q.offset % 4 != 0) return Q4_ERR_MISALIGNED;  // read in quads of elements
+      if (j == 1 && l.n % 4 != 0) return Q4_ERR_UNSUPPORTED_SHAPE;
+      if (q.link >= 0) {
+        if (q.link >= s) return Q4_ERR_INVALID_ARG;  // only earlier links
+        const q4_chain_link& t = links[q.link];
+        const int64_t out_len = (t.ops & Q4_OP_SWIGLU) ? t.n / 2 : t.n;
+        if (q.offset + len[j] > out_len) return Q4_ERR_INVALID_ARG;
+      } else {
+        if (q.ptr == nullptr) return Q4_ERR_INVALID_ARG;
+        if (!aligned(q.ptr, 16)) return Q4_ERR_MISALIGNED;
+      }
+      if (A != nullptr) {
+        A->L[s].ext[j] = q.link >= 0 ? nullptr : q.ptr;
+        A->L[s].src_link[j] = q.link;
+        A->L[s].src_off[j] = q.offset;
+      }
+    }
+    if (l.ops & Q4_OP_ARGMAX) {
+      if (A != nullptr) A->L[s].rec0 = slots_total * kSlotFloats + rec_floats;
+      rec_floats += 2 * C;
+    }
+    kmax = std::max<int>(kmax, static_cast<int>(l.k));
+    slot += static_cast<uint32_t>(groups + C);
+  }
+  const uint64_t set_floats = (uint64_t(slots_total) * kSlotFloats + rec_floats + 63) / 64 * 64;
+  *ws = kHeaderBytes + 2 * set_floats * 4;
+  if (A != nullptr) {
+    A->n_links = n;
+    A->kmax = kmax;
+    A->set_floats = static_cast<uint32_t>(set_floats);
+    A->divC = make_div(C);
+  }
+  return Q4_OK;
+}
+
+size_t chain_smem_bytes(int kmax) {
+  return static_cast<size_t>((rt::xpad_floats(kmax) * 4 + 127) / 128 * 128) +
+         static_cast<size_t>(kWarps) * kStages * rt::kTileBytes;
+}
+
+cudaError_t chain_launch(ChainArgs& A, void* workspace, cudaStream_t s) {
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  A.hdr = reinterpret_cast<uint32_t*>(w);
+  A.set[0] = reinterpret_cast<float*>(w + kHeaderBytes);
+  A.set[1] = A.set[0] + A.set_floats;
+  const size_t smem = chain_smem_bytes(A.kmax);
+  static bool configured[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(chain_smem_bytes(kMaxK)));
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(sm_count()));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;  // every CTA resident: CTAs wait on each other
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, chain_kernel, A);
+}
+
+cudaError_t repack_launch(const uint8_t* W, int64_t n, int64_t k, uint8_t* R, cudaStream_t s) {
+  const int64_t work = (n + 15) / 16 * 16 * (k / 32);
+  const int64_t blocks = (work + 255) / 256;
+  if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  repack_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(W, n, k, R);
+  return cudaGetLastError();
+}
+
+}  // namespace q4
+
+// ------------------------------------------------------------------ C ABI
+extern "C" {
+
+size_t q4_repack_bytes(int64_t n, int64_t k) {
+  if (n <= 0 || k <= 0 || k % 256 != 0 || n > (int64_t(1) << 40) || k > (int64_t(1) << 40))
+    return 0;
+  return static_cast<size_t>((n + 15) / 16 * (k / 256)) * q4::rt::kTileBytes;
+}
+
+q4_status q4_repack(const void* W, int64_t n, int64_t k, void* R, q4_stream_t s) {
+  if (W == nullptr || R == nullptr || n <= 0 || k <= 0 || n > (int64_t(1) << 40) ||
+      k > (int64_t(1) << 40))
+    return Q4_ERR_INVALID_ARG;
+  if (k % 256 != 0) return Q4_ERR_UNSUPPORTED_SHAPE;
+  if (!q4::aligned(W, 16) || !q4::aligned(R, 16)) return Q4_ERR_MISALIGNED;
+  return q4::repack_launch(static_cast<const uint8_t*>(W), n, k, static_cast<uint8_t*>(R),
+                           reinterpret_cast<cudaStream_t>(s)) == cudaSuccess
+             ? Q4_OK
+             : Q4_ERR_CUDA;
+}
+
+size_t q4_chain_workspace_bytes(const q4_chain_link* links, int32_t n_links) {
+  size_t ws = 0;
+  return q4::chain_plan(links, n_links, nullptr, &ws) == Q4_OK ? ws : 0;
+}
+
+q4_status q4_chain(const q4_chain_link* links, int32_t n_links, void* workspace, size_t ws_bytes,
+                   int32_t* status_dev, uint32_t flags, q4_stream_t s) {
+  static thread_local q4::ChainArgs A;  // ~14 KB: kept off the stack
+  size_t need = 0;
+  q4_status st = q4::chain_plan(links, n_links, &A, &need);
+  if (st != Q4_OK) return st;
+  if (workspace == nullptr || ws_bytes < need) return Q4_ERR_WORKSPACE;
+  if (!q4::aligned(workspace, 256)) return Q4_ERR_MISALIGNED;
+  A.status = status_dev;
+  A.flags = flags;
+  return q4::chain_launch(A, workspace, reinterpret_cast<cudaStream_t>(s)) == cudaSuccess
+             ? Q4_OK
+             : Q4_ERR_CUDA;
+}
+
+static q4_chain_link one_link(const void* R, int64_t n, int64_t k, const float* x, float* y) {
+  q4_chain_link l = {};
+  l.R = R;
+  l.n = n;
+  l.k = k;
+  l.x.ptr = x;
+  l.x.link = -1;
+  l.residual.link = -1;
+  l.y = y;
+  return l;
+}
+
+size_t q4_gemv_r_workspace_bytes(int64_t n, int64_t k) {
+  const q4_chain_link l = one_link(reinterpret_cast<const void*>(16), n, k,
+                                   reinterpret_cast<const float*>(16), nullptr);
+  return q4_chain_workspace_bytes(&l, 1);
+}
+
+q4_status q4_gemv_r(const void* R, int64_t n, int64_t k, const float* x, float* y, void* workspace,
+                    size_t ws_bytes, int32_t* status_dev, uint32_t flags, q4_stream_t s) {
+  if (x == nullptr || y == nullptr) return Q4_ERR_INVALID_ARG;
+  const q4_chain_link l = one_link(R, n, k, x, y);
+  return q4_chain(&l, 1, workspace, ws_bytes, status_dev, flags, s);
+}
+
+}  // extern "C"

@@ -26,7 +26,9 @@ from __future__ import annotations
 
 import synth
 
-from . import FLAG_PDL, Workspace, q4_gemm, q4_gemv, q4_gemv_chain, q4_quantize
+from . import (FLAG_PDL, OP_RESIDUAL, OP_SWIGLU, Link, LinkOut, Workspace,
+               interleave_gate_rows, q4_chain, q4_chain_workspace_bytes, q4_gemm, q4_gemv,
+               q4_gemv_chain, q4_quantize, q4_repack)
 
 
 def _quantize_rows(parts, k, device, torch):
@@ -80,6 +82,21 @@ class DecoderStack:
         self.chain_ws = Workspace(self.device)
         self.chain_ws.get(q4_gemv_chain_workspace_bytes(self.links(self.x)))
         self.graphs = {}
+        # the same weights in the repacked tile layout, for the fused step;
+        # w1 and w3 interleaved 8 rows at a time for the gate epilogue
+        self.R = []
+        for layer in self.W:
+            r = {name: q4_repack(w, *self.shapes[name]) for name, w in layer.items()
+                 if name != "w13"}
+            F = self.FFN
+            w13i = interleave_gate_rows(layer["w13"][:F], layer["w13"][F:])
+            r["w13"] = q4_repack(w13i, *self.shapes["w13"])
+            del w13i
+            self.R.append(r)
+        torch.cuda.synchronize()
+        self.x_fused = torch.empty((1, H), device=self.device)
+        self.fused_ws = Workspace(self.device)
+        self.fused_ws.get(q4_chain_workspace_bytes(self.fused_links(self.x_fused)))
 
     # bytes the method must move per decode step (weights once + activations)
     def weight_bytes(self) -> int:
@@ -116,6 +133,48 @@ class DecoderStack:
             out.append((W["w13"], 2 * F, H, self.y_o, self.y_13))
             out.append((W["w2"], H, F, self.y_13[:, :F], self.x))
         return out
+
+    def fused_links(self, x_in, outs=None):
+        """The step as one q4_chain on the repacked weights, with the decoder's
+        glue fused: per layer
+            qkv = Wqkv x_l
+            h   = x_l + Wo q            (q = the first 4096 rows of qkv)
+            g   = a * sigmoid(a) * b,  a = W1 h, b = W3 h  (in the w1/w3 product's epilogue)
+            x_{l+1} = h + W2 g
+        The q rows stand in for the attention output and h for its norm (both
+        outside the Q4 path).  Only x_26 is written (self.x_fused) unless
+        `outs` gives a buffer per link."""
+        H, Q, F = self.HIDDEN, self.QDIM, self.FFN
+        links = []
+        for l in range(self.layers):
+            R, b = self.R[l], 4 * l
+            x_l = x_in if l == 0 else LinkOut(b - 1)
+            y = (lambda i: outs[i]) if outs is not None else (lambda i: None)  # noqa: E731
+            last = l == self.layers - 1
+            links.append(Link(R["qkv"], Q + 2 * self.KVDIM, H, x_l, y=y(b)))
+            links.append(Link(R["wo"], H, Q, LinkOut(b, 0), y=y(b + 1), residual=x_l,
+                              ops=OP_RESIDUAL))
+            links.append(Link(R["w13"], 2 * F, H, LinkOut(b + 1), y=y(b + 2), ops=OP_SWIGLU))
+            links.append(Link(R["w2"], H, F, LinkOut(b + 2), residual=LinkOut(b + 1),
+                              y=(self.x_fused if (last and outs is None) else y(b + 3)),
+                              ops=OP_RESIDUAL))
+        return links
+
+    def fused_step(self, x_in, stream=None, outs=None):
+        q4_chain(self.fused_links(x_in, outs), workspace=self.fused_ws, stream=stream)
+        return self.x_fused
+
+    def capture_fused(self, inputs, stream):
+        """CUDA graph of len(inputs) consecutive fused steps."""
+        torch = self.torch
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            self.fused_step(inputs[0], stream)
+            stream.synchronize()
+            with torch.cuda.graph(g, stream=stream):
+                for x_in in inputs:
+                    self.fused_step(x_in, stream)
+        return g
 
     def step(self, x_in, stream=None, chain: bool = False):
         """One decode step on the device: x_in [1, 3072] fp32 -> self.x [1, 3072].

@@ -205,6 +205,97 @@ size_t q4_gemm_workspace_bytes(int64_t n, int64_t k, int64_t m);
 q4_status q4_embed_gather(const void* table, int64_t vocab, int64_t k, const int32_t* ids,
                           int64_t n_ids, float* out, int32_t* status_dev, q4_stream_t s);
 
+/* ---------------------------------------------------------------------------
+ * Repacked layout and the decode-step chain.
+ *
+ * q4_repack copies a GGUF Q4_0 matrix into this library's GPU layout (the pages
+ * name only the GGUF format, "Arquitectura"; the layout below is a packaging
+ * choice, every block's bytes are kept): rows in groups of 16, k in slices of
+ * 256 (8 blocks); tile (g, t) = rows 16g..16g+15 x blocks 8t..8t+7 is 2304
+ * bytes at (g * k/256 + t) * 2304; inside it, for lane L = 8h + b (h = 0..3,
+ * b = 0..7) and j = 0..3, the binary16 scale of row 16g + 4h + j, block
+ * 8t + b sits at byte 8L + 2j and its codes at 256 + 512j + 16L as four
+ * little-endian words, nibble m of word u holding element 16 (u / 2) + 2m +
+ * (u % 2) of the block.
+ * Rows past n in the last group are d = +0 with every code 8.  Each tile is
+ * one contiguous 16-byte-aligned run that a warp reads in whole 16-byte words.
+ *   W  GGUF Q4_0 [n rows of k/32 blocks], 16-byte aligned; k % 256 == 0.
+ *   R  output, q4_repack_bytes(n, k) bytes, 16-byte aligned, must not overlap W.
+ * q4_repack_bytes returns 0 for a shape it does not take. */
+size_t q4_repack_bytes(int64_t n, int64_t k);
+q4_status q4_repack(const void* W, int64_t n, int64_t k, void* R, q4_stream_t s);
+
+/* Where a chain link reads a vector: the output of an earlier link of the same
+ * chain (link >= 0; elements [offset, offset + len) of that output), or fp32
+ * device memory (link < 0; ptr 16-byte aligned, read when the link starts).
+ * offset is a multiple of 4 elements. */
+typedef struct q4_chain_src {
+  const float* ptr;
+  int32_t link;
+  int32_t offset;
+} q4_chain_src;
+
+/* Q4_OP_SWIGLU: the gated FFN unit in the epilogue of the w1/w3 product.  The
+ * link's n rows (n % 16 == 0) come in 16-row groups of 8 gate rows followed by
+ * the 8 matching up rows (w1 and w3 interleaved 8 rows at a time), and its
+ * output has n/2 elements: out[8g + j] = a * sigmoid(a) * b with a = row
+ * 16g + j and b = row 16g + 8 + j (j < 8).  Not combined with the others. */
+#define Q4_OP_SWIGLU 1u
+#define Q4_OP_RESIDUAL 2u /* y = W x + residual */
+#define Q4_OP_ARGMAX 4u   /* argmax[0] = index of the largest y, argmax[1] = its bits */
+
+/* One batch-1 product of a chain: y = W x (+ residual), fp32. */
+typedef struct q4_chain_link {
+  const void* R;           /* q4_repack layout, n rows, k columns, k % 256 == 0, k <= 12288 */
+  int64_t n, k;
+  q4_chain_src x;          /* k elements */
+  q4_chain_src residual;   /* Q4_OP_RESIDUAL: n elements (from memory: n % 4 == 0) */
+  float* y;                /* output (n fp32, n/2 with Q4_OP_SWIGLU), 4-byte aligned, or NULL */
+  int32_t* argmax;         /* Q4_OP_ARGMAX: [2] int32, 4-byte aligned */
+  uint32_t ops;            /* Q4_OP_* */
+  uint32_t reserved;
+} q4_chain_link;
+
+#define Q4_CHAIN_MAX_LINKS 128
+
+/* A decode step's chain of dependent batch-1 products in one launch.  The
+ * decoder of the Voxtral Mini 4B Realtime port ("Arquitectura": 26 layers,
+ * hidden 3072, GQA 32Q/8KV) runs per token qkv, wo, the gated FFN pair and w2
+ * per layer, each reading an earlier product's output, and its output head,
+ * whose largest logit is the next token.  Links run as if one after another:
+ *   p_s[r] = sum_j w^_s[r][j] x_s[j],  x_s = src(x)
+ *   y_s = p_s (+ src(residual)), or the gated pairs of p_s with Q4_OP_SWIGLU
+ * Each p_s is within 1e-4 * (sum_j |w^ x_s| + |residual|) of the exact value
+ * for the x_s it read; sums over split work are added in a fixed order, so
+ * results do not depend on timing, and a y_s written to memory is bitwise the
+ * value later links read.  Q4_OP_ARGMAX writes the index of the largest y
+ * (lowest index among equal values; NaN never wins; -1 if every y is NaN) and
+ * its value, whether or not y itself is written.  Sigmoid: fp32 exp.
+ *   links      host array of n_links (1..Q4_CHAIN_MAX_LINKS), read during the
+ *              call only.
+ *   workspace  q4_chain_workspace_bytes() bytes, 256-byte aligned, zero-filled
+ *              before its first use and after any call that reported a device
+ *              error; otherwise passed unchanged from call to call (it carries
+ *              a launch counter and the hand-off slots).  Calls that may run
+ *              concurrently need separate workspaces; a chain of a new shape
+ *              is fine on a used workspace (its first call is a little slower).
+ * The launch is cooperative (one CTA per SM, all resident): Q4_ERR_CUDA if the
+ * GPU cannot hold them.  A shape whose per-SM bookkeeping would not fit the
+ * kernel's shared memory returns Q4_ERR_UNSUPPORTED_SHAPE (n up to ~2.6
+ * million rows at k = 3072 fit; with a residual, ~470 thousand). */
+size_t q4_chain_workspace_bytes(const q4_chain_link* links, int32_t n_links);
+q4_status q4_chain(const q4_chain_link* links, int32_t n_links, void* workspace, size_t ws_bytes,
+                   int32_t* status_dev, uint32_t flags, q4_stream_t s);
+
+/* Batch-1 product y = W x on a repacked matrix (a one-link q4_chain): the
+ * per-token product of the decoder linears and the output head
+ * ("Arquitectura").  Same error bound, workspace rules and x alignment as
+ * q4_chain; y [n] fp32, 4-byte aligned. */
+size_t q4_gemv_r_workspace_bytes(int64_t n, int64_t k);
+q4_status q4_gemv_r(const void* R, int64_t n, int64_t k, const float* x, float* y,
+                    void* workspace, size_t ws_bytes, int32_t* status_dev, uint32_t flags,
+                    q4_stream_t s);
+
 /* Linear layer with the batch-size crossover: m <= q4_linear_crossover_m(n, k)
  * and fp32 X run q4_gemv; otherwise q4_gemm (fp32 X is first rounded to bf16
  * into the workspace).  Y is fp32 [m][ldy].  X dtype Q4_F32 needs ldx % 4 == 0,

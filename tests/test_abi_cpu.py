@@ -58,6 +58,9 @@ def test_constants_match_header(q4):
     assert consts["Q4_BLOCK_ELEMS"] == 32 and consts["Q4_BLOCK_BYTES"] == 18
     assert consts["Q4_GEMV_MAX_M"] == q4.GEMV_MAX_M
     assert consts["Q4_FLAG_PDL"] == q4.FLAG_PDL
+    assert consts["Q4_OP_SWIGLU"] == q4.OP_SWIGLU and consts["Q4_OP_RESIDUAL"] == q4.OP_RESIDUAL
+    assert consts["Q4_OP_ARGMAX"] == q4.OP_ARGMAX
+    assert consts["Q4_CHAIN_MAX_LINKS"] == q4.CHAIN_MAX_LINKS
 
 
 def test_status_strings(q4):
@@ -120,6 +123,62 @@ def test_host_validation_rejects_bad_arguments(q4):
     assert L.q4_gemv_noalloc(A16, 8, 64, A16, 1, 32, A16, 8, None, 0, None) == q4.ERR_INVALID_ARG
     assert L.q4_gemv_noalloc(A16, 8, 64, A2, 1, 64, A16, 8, None, 0, None) == q4.ERR_MISALIGNED
     assert L.q4_gemv_noalloc(A16, 8, 64, A16, 2, 66, A16, 8, None, 0, None) == q4.ERR_MISALIGNED
+
+
+def _bad_link(q4, **kw):
+    from bit_weight_quantized_03_b300._lib import ChainLink
+    arr = (ChainLink * 2)()
+    for a in arr:
+        a.R, a.n, a.k = A16, 64, 256
+        a.x.ptr, a.x.link, a.x.offset = A16, -1, 0
+        a.residual.link = -1
+        a.y, a.ops = A16, 0
+    for key, v in kw.items():
+        obj, field = (arr[1], key) if "." not in key else (getattr(arr[1], key.split(".")[0]),
+                                                           key.split(".")[1])
+        setattr(obj, field, v)
+    return arr
+
+
+def test_repacked_and_chain_host_validation(q4):
+    L = q4.lib()
+    assert L.q4_repack_bytes(4, 288) == 0
+    assert L.q4_repack_bytes(17, 256) == 2 * 2304
+    assert L.q4_repack_bytes(16, 512) == 2 * 2304
+    assert L.q4_repack(None, 4, 256, A16, None) == q4.ERR_INVALID_ARG
+    assert L.q4_repack(A16, 4, 288, A16, None) == q4.ERR_UNSUPPORTED_SHAPE
+    assert L.q4_repack(A2, 4, 256, A16, None) == q4.ERR_MISALIGNED
+    assert L.q4_gemv_r_workspace_bytes(4096, 3072) > 0
+    assert L.q4_gemv_r_workspace_bytes(4096, 3000) == 0
+    good = _bad_link(q4)
+    assert L.q4_chain_workspace_bytes(good, 2) > 0
+    cases = [
+        (dict(k=288), q4.ERR_UNSUPPORTED_SHAPE),            # k % 256
+        (dict(k=12544), q4.ERR_UNSUPPORTED_SHAPE),          # k above the kernel's limit
+        (dict(R=A2), q4.ERR_MISALIGNED),
+        (dict(R=None), q4.ERR_INVALID_ARG),
+        (dict(n=0), q4.ERR_INVALID_ARG),
+        (dict(ops=8), q4.ERR_INVALID_ARG),                   # unknown op
+        (dict(ops=q4.OP_ARGMAX), q4.ERR_INVALID_ARG),        # argmax without an output
+        (dict(**{"x.link": 1}), q4.ERR_INVALID_ARG),         # not an earlier link
+        (dict(**{"x.link": 0, "x.offset": 2}), q4.ERR_MISALIGNED),   # offset % 4
+        (dict(**{"x.link": 0, "x.offset": 16}), q4.ERR_INVALID_ARG),  # past the source's n
+        (dict(**{"x.ptr": A16 + 4}), q4.ERR_MISALIGNED),
+        (dict(**{"x.offset": 2}), q4.ERR_MISALIGNED),
+        (dict(ops=q4.OP_SWIGLU, n=72), q4.ERR_INVALID_ARG),  # gate rows: n % 16
+        (dict(ops=q4.OP_SWIGLU | q4.OP_RESIDUAL, **{"residual.ptr": A16}),
+         q4.ERR_INVALID_ARG),                                # the gate stands alone
+        (dict(ops=q4.OP_RESIDUAL, n=62, **{"residual.ptr": A16}), q4.ERR_UNSUPPORTED_SHAPE),
+    ]
+    for kw, want in cases:
+        arr = _bad_link(q4, **kw)
+        assert L.q4_chain(arr, 2, A16, 1 << 30, None, 0, None) == want, kw
+        assert L.q4_chain_workspace_bytes(arr, 2) == 0, kw
+    assert L.q4_chain(good, 0, A16, 1 << 30, None, 0, None) == q4.ERR_INVALID_ARG
+    assert L.q4_chain(good, 129, A16, 1 << 30, None, 0, None) == q4.ERR_INVALID_ARG
+    assert L.q4_chain(good, 2, None, 0, None, 0, None) == q4.ERR_WORKSPACE
+    assert L.q4_chain(good, 2, A16, 16, None, 0, None) == q4.ERR_WORKSPACE
+    assert L.q4_chain(good, 2, A16 + 16, 1 << 30, None, 0, None) == q4.ERR_MISALIGNED
 
 
 def test_workspace_sizes_are_consistent(q4):
