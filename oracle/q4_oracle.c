@@ -285,15 +285,29 @@ int64_t q4o_repack_bytes(int64_t n, int64_t k) {
   return groups * (k / 256) * 2304;
 }
 
-/* Byte offsets of block (row r, block kb) inside the repacked matrix. */
-static void q4o_tile_offsets(int64_t r, int64_t kb, int64_t k, int64_t* scale_off,
-                             int64_t* code_off) {
-  int64_t g = r / 16, t = kb / 8;
-  int64_t h = (r % 16) / 4, j = r % 4, b = kb % 8;
-  int64_t lane = 8 * h + b;
-  int64_t tile = (g * (k / 256) + t) * 2304;
-  *scale_off = tile + 8 * lane + 2 * j;
-  *code_off = tile + 256 + 512 * j + 16 * lane;
+/* Byte offsets, inside the repacked matrix, of element e (0..31) of block kb
+ * of row r: its binary16 scale (2 bytes) and the byte holding its code, with
+ * *high = 1 when the code is that byte's high nibble.  The layout is the one
+ * q4.h defines: tile (r / 16, kb / 8) of 2304 bytes; rows 16G + g and
+ * 16G + g + 8 (g = 0..7) pair up; a tile's column c = 16s + i (s = 0..15) sits
+ * with lane L = 4g + (i % 8) / 2 of step s, as nibble
+ * m = hr + 2 (i / 8) + 4 (i % 2) of that lane's step word (hr = 1 for the row
+ * g + 8). */
+static void q4o_tile_offsets(int64_t r, int64_t kb, int64_t e, int64_t k, int64_t* scale_off,
+                             int64_t* code_off, int* high) {
+  int64_t tile = ((r / 16) * (k / 256) + kb / 8) * 2304;
+  int64_t rr = r % 16, g = rr % 8, hr = rr / 8, b = kb % 8;
+  int64_t s = 2 * b + e / 16, i = e % 16;
+  int64_t lane = 4 * g + (i % 8) / 2;
+  int64_t m = hr + 2 * (i / 8) + 4 * (i % 2);
+  *scale_off = tile + 32 * g + 4 * b + 2 * hr;
+  *code_off = tile + 256 + 512 * (s / 4) + 16 * lane + 4 * (s % 4) + m / 2;
+  *high = (int)(m % 2);
+}
+
+static void q4o_put_nibble(uint8_t* byte, int high, int q) {
+  if (high) *byte = (uint8_t)((*byte & 0x0F) | (q << 4));
+  else *byte = (uint8_t)((*byte & 0xF0) | q);
 }
 
 int q4o_repack(const uint8_t* W, int64_t n, int64_t k, uint8_t* R) {
@@ -301,26 +315,19 @@ int q4o_repack(const uint8_t* W, int64_t n, int64_t k, uint8_t* R) {
   int64_t nb = k / 32, groups = (n + 15) / 16;
   for (int64_t r = 0; r < groups * 16; ++r) {
     for (int64_t kb = 0; kb < nb; ++kb) {
-      int64_t so, co;
-      q4o_tile_offsets(r, kb, k, &so, &co);
-      if (r >= n) { /* padding row: d = +0, every code 8 */
-        R[so] = 0;
-        R[so + 1] = 0;
-        memset(R + co, 0x88, 16);
-        continue;
-      }
-      const uint8_t* blk = W + (r * nb + kb) * 18;
-      uint8_t q[32];
-      for (int c = 0; c < 16; ++c) {
-        q[c] = blk[2 + c] & 0x0F;
-        q[c + 16] = (blk[2 + c] >> 4) & 0x0F;
-      }
-      R[so] = blk[0];
-      R[so + 1] = blk[1];
-      for (int c = 0; c < 16; ++c) {
-        int u = c / 4, i = c % 4;
-        int e = 16 * (u / 2) + 4 * i + (u % 2); /* low nibble; high nibble: e + 2 */
-        R[co + c] = (uint8_t)(q[e] | (q[e + 2] << 4));
+      const uint8_t* blk = r < n ? W + (r * nb + kb) * 18 : NULL;
+      for (int e = 0; e < 32; ++e) {
+        int64_t so, co;
+        int high;
+        q4o_tile_offsets(r, kb, e, k, &so, &co, &high);
+        /* padding rows past n: d = +0 and every code 8 */
+        int q = 8;
+        if (blk) q = e < 16 ? (blk[2 + e] & 0x0F) : (blk[2 + e - 16] >> 4);
+        q4o_put_nibble(R + co, high, q);
+        if (e == 0) {
+          R[so] = blk ? blk[0] : 0;
+          R[so + 1] = blk ? blk[1] : 0;
+        }
       }
     }
   }
@@ -332,19 +339,18 @@ int q4o_unrepack(const uint8_t* R, int64_t n, int64_t k, uint8_t* W) {
   int64_t nb = k / 32;
   for (int64_t r = 0; r < n; ++r) {
     for (int64_t kb = 0; kb < nb; ++kb) {
-      int64_t so, co;
-      q4o_tile_offsets(r, kb, k, &so, &co);
       uint8_t* blk = W + (r * nb + kb) * 18;
-      uint8_t q[32];
-      for (int c = 0; c < 16; ++c) {
-        int u = c / 4, i = c % 4;
-        int e = 16 * (u / 2) + 4 * i + (u % 2);
-        q[e] = R[co + c] & 0x0F;
-        q[e + 2] = (R[co + c] >> 4) & 0x0F;
+      for (int e = 0; e < 32; ++e) {
+        int64_t so, co;
+        int high;
+        q4o_tile_offsets(r, kb, e, k, &so, &co, &high);
+        int q = high ? (R[co] >> 4) : (R[co] & 0x0F);
+        if (e == 0) {
+          blk[0] = R[so];
+          blk[1] = R[so + 1];
+        }
+        q4o_put_nibble(blk + 2 + (e % 16), e >= 16, q);
       }
-      blk[0] = R[so];
-      blk[1] = R[so + 1];
-      for (int c = 0; c < 16; ++c) blk[2 + c] = (uint8_t)(q[c] | (q[c + 16] << 4));
     }
   }
   return Q4O_OK;

@@ -93,16 +93,19 @@ int64_t q4o_argmax(const double* y, int64_t n);
  * the pages name only the GGUF format).  Definition, for k % 256 == 0:
  *   rows are taken in groups of 16 (the last group padded with rows whose
  *   blocks have d = +0 and every code 8), k in slices of 256 (8 blocks);
- *   tile (g, t) = rows 16g..16g+15 x blocks 8t..8t+7 is 2304 bytes at offset
- *   (g * (k/256) + t) * 2304;
- *   inside a tile, lane L = 8h + b (h = 0..3, b = 0..7) stands for rows
- *   16g + 4h + j (j = 0..3) of block 8t + b:
- *     bytes [8L + 2j, 8L + 2j + 2): that block's binary16 d, little-endian;
- *     bytes [256 + 512j + 16L, +16): its codes as four little-endian 32-bit
- *     words; nibble m (bits 4m..4m+3) of word u holds element
- *     16 (u / 2) + 2m + (u % 2), i.e. byte c = 4u + i holds element
- *     16 (u / 2) + 4i + (u % 2) in its low nibble and that element + 2 in its
- *     high nibble.
+ *   tile (G, t) = rows 16G..16G+15 x blocks 8t..8t+7 is 2304 bytes at offset
+ *   (G * (k/256) + t) * 2304.  Inside a tile, with g = 0..7 and hr = 0 for row
+ *   16G + g, hr = 1 for row 16G + g + 8:
+ *     scales: bytes [32g + 4b + 2hr, +2) hold the binary16 d of that row's
+ *       block 8t + b, little-endian;
+ *     codes: the tile's 256 columns are 16 steps of 16 (column c = 16s + i);
+ *       lane L = 4g + (i % 8) / 2 of step s owns a little-endian 32-bit word
+ *       at 256 + 512 (s / 4) + 16L + 4 (s % 4), whose nibble
+ *       m = hr + 2 (i / 8) + 4 (i % 2) (bits 4m..4m+3) holds the code of
+ *       column c.  So a byte of a word holds rows g (low nibble) and g + 8
+ *       (high nibble) of one column, and the word holds a lane's four columns
+ *       2(i%8/2) + {0, 1, 8, 9} of the step: the operand order of a 16 x 16
+ *       row-major tensor-core A fragment.
  * q4o_repack_bytes gives the size; q4o_repack / q4o_unrepack convert (the
  * padding rows are dropped by q4o_unrepack).  Return Q4O_OK or
  * Q4O_ERR_INVALID_ARG. */

@@ -35,14 +35,16 @@ MUTANTS = {
     "argmax_last_tie": ("if (best < 0 || y[i] > y[best]) best = i;",
                         "if (best < 0 || y[i] >= y[best]) best = i;"),
     "argmax_keeps_nan": ("if (isnan(y[i])) continue;", "if (0) continue;"),
-    "repack_lane_order": ("int64_t lane = 8 * h + b;", "int64_t lane = 4 * b + h;"),
-    "repack_gguf_nibbles": ("R[co + c] = (uint8_t)(q[e] | (q[e + 2] << 4));",
-                            "R[co + c] = (uint8_t)(q[c] | (q[c + 16] << 4));"),
-    "repack_pair_order": ("int e = 16 * (u / 2) + 4 * i + (u % 2); /* low nibble; high nibble: e + 2 */",
-                          "int e = 16 * (u / 2) + 4 * i + (u % 2) * 2; /* low nibble; high nibble: e + 2 */"),
-    "repack_scale_slot": ("*scale_off = tile + 8 * lane + 2 * j;",
-                          "*scale_off = tile + 2 * lane + 64 * j;"),
-    "repack_pad_code": ("memset(R + co, 0x88, 16);", "memset(R + co, 0x00, 16);"),
+    "repack_lane_order": ("int64_t lane = 4 * g + (i % 8) / 2;", "int64_t lane = 4 * g + (i % 4);"),
+    "repack_nibble_order": ("int64_t m = hr + 2 * (i / 8) + 4 * (i % 2);",
+                            "int64_t m = 2 * hr + (i / 8) + 4 * (i % 2);"),
+    "repack_gguf_nibbles": ("if (blk) q = e < 16 ? (blk[2 + e] & 0x0F) : (blk[2 + e - 16] >> 4);",
+                            "if (blk) q = (e % 2) ? (blk[2 + e / 2] >> 4) : (blk[2 + e / 2] & 0x0F);"),
+    "repack_step_word": ("*code_off = tile + 256 + 512 * (s / 4) + 16 * lane + 4 * (s % 4) + m / 2;",
+                         "*code_off = tile + 256 + 512 * (s % 4) + 16 * lane + 4 * (s / 4) + m / 2;"),
+    "repack_scale_slot": ("*scale_off = tile + 32 * g + 4 * b + 2 * hr;",
+                          "*scale_off = tile + 32 * b + 4 * g + 2 * hr;"),
+    "repack_pad_code": ("int q = 8;", "int q = 0;"),
     "f64_rounds_x": ("double p = (double)wrow[kk] * x[kk];",
                      "double p = (double)wrow[kk] * (double)(float)x[kk];"),
 }

@@ -39,15 +39,15 @@ def test_repack_hand_derived_offsets(oracle_mod):
     R = oracle_mod.repack(W, n, k)
     assert R.size == oracle_mod.repack_bytes(n, k) == 9216
     rows = read_golden("repack_offsets.txt")
-    assert len(rows) == 6
+    assert len(rows) == 7
     for row, blk, el, so, co, half in rows:
         r, kb, e, so, co = int(row), int(blk), int(el), int(so), int(co)
         assert R[so] == W[r, kb * 18] and R[so + 1] == W[r, kb * 18 + 1], (r, kb)
         got = int(R[co] & 0xF) if half == "low" else int(R[co] >> 4)
         assert got == _nibble(W, k // 32, r, kb, e), (r, kb, e)
     # padding row 31, block 0 (hand-derived in the golden file's comments)
-    assert R[4806] == 0 and R[4807] == 0
-    assert np.all(R[6784:6800] == 0x88)
+    assert R[4834] == 0 and R[4835] == 0
+    assert np.all(R[5312:5320] == 0x88)
 
 
 @pytest.mark.parametrize("n,k", [(1, 256), (16, 256), (37, 768), (64, 3072)])
