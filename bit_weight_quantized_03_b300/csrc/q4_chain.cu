@@ -12,12 +12,13 @@
 // products, of which there are 104 per step.
 //
 // Design (one cooperative launch, one 16-warp CTA per SM):
-//   * Weights are read in the repacked 16-row x 256-column tiles (2304 bytes,
-//     q4r_tile.cuh) with one 1-D bulk copy per tile.  Link s's T tiles are cut
-//     into contiguous CTA ranges [T c / C, T (c+1) / C), each CTA range into 16
-//     contiguous warp ranges.  Each warp streams its own tiles through a ring of
-//     four slots and runs ahead into later links while it waits, so the weight
-//     stream does not stop at a hand-off.
+//   * Weights are read in the repacked 16-row x 256-column tiles
+//     (q4r_tile.cuh) and multiplied on the tensor cores (mma.m16n8k16, f16
+//     operands decoded exactly from the codes, fp32 accumulation).  Link s's
+//     T tiles are cut into contiguous CTA ranges, each CTA range into 16
+//     contiguous warp ranges.  Each warp streams its own tiles, two per bulk
+//     copy, through a ring of two slots and runs ahead into later links while
+//     it waits, so the weight stream does not stop at a hand-off.
 //   * A warp sums its tiles' row products per 16-row group; at the end of a
 //     link the CTA adds its warps' group sums in warp order and publishes one
 //     partial per (group, CTA) into a slot of 16 floats in the workspace.  The
@@ -25,12 +26,19 @@
 //     residual.  A group is split between at most a few CTAs.
 //   * A link's input is read from the slots of the link that produced it: an
 //     element is the sum of its group's partials in CTA order (so the result
-//     does not depend on timing), and the gated FFN unit x * sigmoid(x) * up is
-//     applied while reading.  There is no grid barrier and no flag: a slot word
-//     holds a NaN pattern that arithmetic never produces until its value is
-//     written, and a reader polls the values themselves.  The workspace keeps
-//     two sets of slots used by alternate launches; each launch puts the set
-//     the next launch will use back to that pattern.
+//     does not depend on timing).  A slot word holds a NaN pattern that
+//     arithmetic never produces until its value is written, and a reader
+//     checks the values themselves; each CTA also counts itself done on a
+//     per-link counter after publishing, and one thread per reader CTA waits
+//     for that count before the CTA reads, so that the slots are not polled by
+//     every thread while the producers still compute.  The workspace keeps two
+//     sets of slots used by alternate launches; each launch puts the set the
+//     next launch will use back to that pattern, and the last CTA to finish
+//     puts the counters back to zero.
+//   * The staged input is split for the tensor cores: each 32-element block is
+//     scaled by a power of two that puts its largest magnitude in
+//     [2^14, 2^15) and carried as a binary16 pair hi + lo (relative error
+//     below 2^-22); the block's inverse scale is applied to the fp32 sums.
 //   * An output with the argmax op is reduced without writing it: each CTA
 //     takes the largest of the rows it finishes, and CTA 0 reduces the CTAs'
 //     records at the end of the launch.
@@ -46,22 +54,25 @@
 namespace q4 {
 namespace {
 
-// 8 warps per SM decode as fast as 16 (the decode is throughput-bound) and
-// leave each thread 255 registers, so the gathers keep every load in flight.
-constexpr int kWarps = 8;
+constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
-constexpr int kStages = 8;           // ring slots per warp (a power of two)
-constexpr int kWarpGroups = 16;      // 16-row groups one warp may touch in one link
+constexpr int kSlots = 2;            // ring slots per warp (a power of two)
+constexpr int kChunk = 2;            // tiles per bulk copy
+constexpr int kChunkBytes = kChunk * rt::kTileBytes;
+constexpr int kWarpGroups = 8;       // 16-row groups one warp may touch in one link
 constexpr int kCtaGroups = 64;       // groups one CTA may first-own in a link with a residual
 constexpr int kMaxLinks = Q4_CHAIN_MAX_LINKS;
 constexpr int kMaxK = 12288;
+constexpr int kStageQuads = 2;       // element quads per thread and staging pass
 constexpr int kSlotFloats = 16;      // one 16-row group partial
 constexpr uint32_t kEmpty = 0x7FBADBADu;  // NaN pattern that no arithmetic produces
-constexpr int kHeaderBytes = 512;
+constexpr int kHeaderBytes = 1024;
 // header words (uint32): epoch, finished-CTA counter, abort flag, reset barrier,
-// clean extent of buffer 0 / 1 (floats), each on its own 64-byte line
+// clean extent of buffer 0 / 1 (floats), each on its own 64-byte line; then
+// one done-CTA counter per link
 constexpr int kHdrEpoch = 0, kHdrFinished = 16, kHdrAbort = 32, kHdrBarrier = 48;
-constexpr int kHdrClean0 = 64, kHdrClean1 = 80;
+constexpr int kHdrClean0 = 64, kHdrClean1 = 80, kHdrCount = 128;
+static_assert(kHdrCount + kMaxLinks <= kHeaderBytes / 4, "header");
 
 // floor(n / d) for 32-bit n by a multiply-high and a shift (constants made on
 // the host), then checked exactly.
@@ -90,6 +101,7 @@ struct ChainLink {
   uint32_t slot0;        // first slot of this link in a slot set
   uint32_t rec0;         // first argmax record (2 floats per CTA) in a slot set
   Div divU;              // division by the number of units (tiles / unit)
+  Div divNsb;            // division by nsb
 };
 
 struct ChainArgs {
@@ -129,6 +141,9 @@ __device__ __forceinline__ void st_relaxed_u32(uint32_t* p, uint32_t v) {
 __device__ __forceinline__ void st_relaxed_f32(float* p, float v) {
   asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(__float_as_uint(v)) : "memory");
 }
+__device__ __forceinline__ void red_relaxed_add(uint32_t* p, uint32_t v) {
+  asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 
 __device__ __forceinline__ bool empty4(const uint4& v) {
   return v.x == kEmpty || v.y == kEmpty || v.z == kEmpty || v.w == kEmpty;
@@ -145,16 +160,24 @@ __device__ __forceinline__ void add4(float4& a, const uint4& v) {
 }
 
 // Per-link data that a CTA reads in its loops, copied from the kernel
-// parameters into shared memory when the launch starts.  A link's work is cut
-// into units of `unit` tiles (a whole 16-row group, or one tile); CTA c holds
-// units [U c / C, U (c+1) / C), i.e. tiles [ca, cb).
+// parameters into shared memory when the launch starts (parameter reads with
+// a link index that varies are constant-cache loads that miss).  A link's work
+// is cut into units of `unit` tiles (a whole 16-row group, or one tile); CTA c
+// holds units [U c / C, U (c+1) / C), i.e. tiles [ca, cb).
 struct SLink {
   const uint8_t* R;
-  float* slots;        // this link's slots in the launch's slot set
+  float* y;
+  int32_t* argmax;
+  const float* ext[2];
+  int32_t src_link[2], src_off[2];
+  uint32_t slot0;      // this link's first slot in a slot set
+  uint32_t rec0;       // its first argmax record
   int32_t ca, cb;      // this CTA's tiles
-  int32_t nsb, n;
+  int32_t nsb, n, k;
   int32_t unit, units;
+  int32_t g0c, gcount; // this CTA's first 16-row group and its number of groups
   Div divU;
+  Div divNsb;          // division by nsb
   uint32_t ops;
 };
 
@@ -190,11 +213,9 @@ __device__ __noinline__ void fail(Ctx& x) {
   }
 }
 
-// True while the bounded wait that started at x.t0 may continue.  A poll that
-// found nothing sleeps a little before the next, so that waiting SMs do not
-// crowd the L2 that the SMs still computing stream their weights through.
+// True while the bounded wait that started at x.t0 may continue.
 __device__ __forceinline__ bool keep_waiting(Ctx& x, int& spins) {
-  __nanosleep(spins < 4 ? 32 : 128);
+  if (spins >= 8) __nanosleep(64);
   if ((++spins & 15) != 0) return true;
   if (*reinterpret_cast<volatile int*>(x.s_abort)) return false;
   if (ld_relaxed_u32(x.hdr + kHdrAbort) != 0u || global_timer_ns() - x.t0 > kWaitLimitNs) {
@@ -204,157 +225,152 @@ __device__ __forceinline__ bool keep_waiting(Ctx& x, int& spins) {
   return true;
 }
 
-// One input of a link, as its reader sees it: slots of an earlier link
-// (slots != nullptr) or a vector in memory (ext).  An output element e of a
-// link sits in group e >> shift at position e & (2^shift - 1) of its slot
-// (shift 4; 3 for a gated link, whose slots hold 8 values).
-struct Src {
-  const float* slots;
-  const float* ext;
-  int32_t off;
-  int32_t nsb, unit, shift;
-  Div divU;
+// Thread 0 waits until every CTA has counted itself done with link s (bounded);
+// the CTA then reads that link's slots.  Called by all threads (barrier).
+__device__ __forceinline__ void wait_link_done(Ctx& x, int s, int tid) {
+  if (s >= 0 && tid == 0) {
+    const uint32_t* cnt = x.hdr + kHdrCount + s;
+    if (ld_relaxed_u32(cnt) < x.C) {
+      x.t0 = global_timer_ns();
+      int sp = 0;
+      while (ld_relaxed_u32(cnt) < x.C)
+        if (!keep_waiting(x, sp)) break;
+    }
+  }
+  __syncthreads();
+}
+
+// An element quad a thread reads before a link: the first of np partials of an
+// earlier link's output (slots kSlotFloats apart, summed in CTA order), or a
+// plain vector in memory (np == 0); np < 0: nothing to read.  Its address is
+// worked out before the thread waits for the producing link, so that only the
+// loads remain once that link is done.
+struct Ent {
+  const float* p;
+  int np;
 };
 
-// Elements [e, e + 4) of NS sources (NS = 1, or 2 for the gate) for up to W
-// entries (e < 0: unused).  A link-output element is the sum of its group's
-// partials in CTA order; the first two CTAs of every entry of every source
-// are polled in one pass, further ones (links with fewer tiles than SMs) one
-// after another.  false on abort.
-template <int W, int NS>
-__device__ __forceinline__ bool gather(const Src (&S)[NS], Ctx& x, const int (&e)[W],
-                                       float4 (&out)[NS][W]) {
-  const float* q[NS][W];
-  int clo[NS][W], chi[NS][W];
-  uint4 v0[NS][W], v1[NS][W];
-  bool d0[NS][W], d1[NS][W];
+// Elements [row, row + 4) of a source: an earlier link's output (src >= 0)
+// or memory at ext.
+__device__ __forceinline__ Ent make_entry(const SLink* sl, float* set_base, const float* ext,
+                                          int src, int row, uint32_t C) {
+  Ent en;
+  if (src < 0) {
+    en.p = ext + row;
+    en.np = 0;
+    return en;
+  }
+  const SLink& T = sl[src];
+  const int shift = (T.ops & kOpSwiglu) ? 3 : 4;
+  const int g = row >> shift;
+  int clo, chi;
+  group_owners(T, g, C, clo, chi);
+  en.p = set_base + static_cast<size_t>(T.slot0 + g + clo) * kSlotFloats +
+         (row & ((1 << shift) - 1));
+  en.np = chi - clo + 1;
+  return en;
+}
+
+// Loads W entries (the first two partials of every entry in one pass,
+// re-read while a value still holds the empty pattern; further partials one
+// after another).  false on abort.
+template <int W>
+__device__ __forceinline__ bool load_entries(const Ent (&en)[W], Ctx& x, float4 (&out)[W]) {
+  uint4 v0[W], v1[W];
+  bool d0[W], d1[W];
 #pragma unroll
-  for (int j = 0; j < NS; ++j) {
-    SLink L;  // only the fields group_owners reads
-    L.nsb = S[j].nsb;
-    L.unit = S[j].unit;
-    L.divU = S[j].divU;
-#pragma unroll
-    for (int m = 0; m < W; ++m) {
-      d0[j][m] = d1[j][m] = true;
-      clo[j][m] = 0;
-      chi[j][m] = -1;
-      q[j][m] = S[j].slots;
-      if (e[m] < 0) continue;
-      if (S[j].slots == nullptr) {
-        out[j][m] = __ldcg(reinterpret_cast<const float4*>(S[j].ext + S[j].off + e[m]));
-        continue;
-      }
-      const int row = S[j].off + e[m], g = row >> S[j].shift;
-      group_owners(L, g, x.C, clo[j][m], chi[j][m]);
-      q[j][m] = S[j].slots + static_cast<size_t>(g + clo[j][m]) * kSlotFloats +
-                (row & ((1 << S[j].shift) - 1));
-      d0[j][m] = false;
-      d1[j][m] = chi[j][m] <= clo[j][m];
-    }
+  for (int m = 0; m < W; ++m) {
+    d0[m] = en[m].np <= 0;
+    d1[m] = en[m].np <= 1;
+    if (en[m].np == 0) out[m] = __ldcg(reinterpret_cast<const float4*>(en[m].p));
   }
   x.t0 = global_timer_ns();
   int spins = 0;
   while (true) {
 #pragma unroll
-    for (int j = 0; j < NS; ++j)
-#pragma unroll
-      for (int m = 0; m < W; ++m) {
-        if (!d0[j][m]) v0[j][m] = ld_relaxed_v4(q[j][m]);
-        if (!d1[j][m]) v1[j][m] = ld_relaxed_v4(q[j][m] + kSlotFloats);
-      }
+    for (int m = 0; m < W; ++m) {
+      if (!d0[m]) v0[m] = ld_relaxed_v4(en[m].p);
+      if (!d1[m]) v1[m] = ld_relaxed_v4(en[m].p + kSlotFloats);
+    }
     bool all = true;
 #pragma unroll
-    for (int j = 0; j < NS; ++j)
-#pragma unroll
-      for (int m = 0; m < W; ++m) {
-        if (!d0[j][m]) d0[j][m] = !empty4(v0[j][m]);
-        if (!d1[j][m]) d1[j][m] = !empty4(v1[j][m]);
-        all = all && d0[j][m] && d1[j][m];
-      }
+    for (int m = 0; m < W; ++m) {
+      if (!d0[m]) d0[m] = !empty4(v0[m]);
+      if (!d1[m]) d1[m] = !empty4(v1[m]);
+      all = all && d0[m] && d1[m];
+    }
     if (all) break;
     if (!keep_waiting(x, spins)) return false;
   }
 #pragma unroll
-  for (int j = 0; j < NS; ++j)
-#pragma unroll
-    for (int m = 0; m < W; ++m) {
-      if (e[m] < 0 || S[j].slots == nullptr) continue;
-      float4 s = as_f4(v0[j][m]);
-      if (chi[j][m] > clo[j][m]) add4(s, v1[j][m]);
-      for (int cc = clo[j][m] + 2; cc <= chi[j][m]; ++cc) {
-        const float* p = q[j][m] + static_cast<size_t>(cc - clo[j][m]) * kSlotFloats;
-        uint4 u;
-        x.t0 = global_timer_ns();
-        int sp = 0;
-        while (true) {
-          u = ld_relaxed_v4(p);
-          if (!empty4(u)) break;
-          if (!keep_waiting(x, sp)) return false;
-        }
-        add4(s, u);
+  for (int m = 0; m < W; ++m) {
+    if (en[m].np < 1) continue;
+    float4 s = as_f4(v0[m]);
+    if (en[m].np > 1) add4(s, v1[m]);
+    for (int cc = 2; cc < en[m].np; ++cc) {
+      const float* p = en[m].p + static_cast<size_t>(cc) * kSlotFloats;
+      uint4 u;
+      x.t0 = global_timer_ns();
+      int sp = 0;
+      while (true) {
+        u = ld_relaxed_v4(p);
+        if (!empty4(u)) break;
+        if (!keep_waiting(x, sp)) return false;
       }
-      out[j][m] = s;
+      add4(s, u);
     }
+    out[m] = s;
+  }
   return true;
+}
+
+// The x entries of staging pass `pass`: element quads tid + (pass W + m) kThreads.
+__device__ __forceinline__ void x_entries(const SLink* sl, float* set_base, const SLink& S,
+                                          int pass, int tid, uint32_t C,
+                                          Ent (&en)[kStageQuads + 1]) {
+  const int quads = S.k / 4;
+#pragma unroll
+  for (int m = 0; m < kStageQuads; ++m) {
+    const int q = tid + (pass * kStageQuads + m) * kThreads;
+    en[m].np = -1;
+    if (q < quads) en[m] = make_entry(sl, set_base, S.ext[0], S.src_link[0], S.src_off[0] + 4 * q, C);
+  }
 }
 
 __device__ __forceinline__ float silu_gate(float a, float b) { return a / (1.0f + __expf(-a)) * b; }
 
-// Stage x of a link into shared memory (padded layout).
-template <int W>
-__device__ __forceinline__ bool stage_x(const Src& a, int k, float* xs, Ctx& x, int tid0,
-                                        int nthr) {
-  const int quads = k / 4;
-  const Src S[1] = {a};
-  for (int q0 = tid0; q0 < quads; q0 += nthr * W) {
-    int e[W];
+// Staged x for the tensor cores: every 32-element block scaled by a power of
+// two and split into binary16 hi + lo (q4r_tile.cuh layout), its inverse
+// scale in xinv.  The eight lanes 8j..8j+7 of a warp hold the eight quads of
+// one block (kThreads and the pass stride are multiples of 8).
+__device__ __forceinline__ void convert_x(const float4 (&v)[kStageQuads + 1],
+                                          const Ent (&en)[kStageQuads + 1], int pass, int tid,
+                                          uint8_t* x16, float* xinv) {
 #pragma unroll
-    for (int m = 0; m < W; ++m) {
-      const int q = q0 + m * nthr;
-      e[m] = q < quads ? 4 * q : -1;
-    }
-    float4 v[1][W];
-    if (!gather<W, 1>(S, x, e, v)) return false;
-#pragma unroll
-    for (int m = 0; m < W; ++m)
-      if (e[m] >= 0) *reinterpret_cast<float4*>(xs + rt::xpad(e[m])) = v[0][m];
+  for (int m = 0; m < kStageQuads; ++m) {
+    const bool valid = en[m].np >= 0;
+    const int e = 4 * (tid + (pass * kStageQuads + m) * kThreads);
+    float amax = valid ? fmaxf(fmaxf(fabsf(v[m].x), fabsf(v[m].y)),
+                               fmaxf(fabsf(v[m].z), fabsf(v[m].w)))
+                       : 0.f;
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+    if (!valid) continue;
+    float sc, inv;
+    rt::block_scale(amax, sc, inv);
+    __half h[4], l[4];
+    rt::split_hi_lo(v[m].x * sc, h[0], l[0]);
+    rt::split_hi_lo(v[m].y * sc, h[1], l[1]);
+    rt::split_hi_lo(v[m].z * sc, h[2], l[2]);
+    rt::split_hi_lo(v[m].w * sc, h[3], l[3]);
+    const int s = e >> 4, i0 = e & 15;
+    *reinterpret_cast<__half2*>(x16 + rt::x16_word(s, 0, i0)) = __halves2half2(h[0], h[1]);
+    *reinterpret_cast<__half2*>(x16 + rt::x16_word(s, 0, i0 + 2)) = __halves2half2(h[2], h[3]);
+    *reinterpret_cast<__half2*>(x16 + rt::x16_word(s, 1, i0)) = __halves2half2(l[0], l[1]);
+    *reinterpret_cast<__half2*>(x16 + rt::x16_word(s, 1, i0 + 2)) = __halves2half2(l[2], l[3]);
+    if ((tid & 7) == 0) xinv[e >> 5] = inv;
   }
-  return true;
-}
-
-// Residual rows of the groups this CTA holds the first tile of -> sres[gl][row]
-// (gl = group - g0c); rows past n read as zero.
-__device__ __forceinline__ bool stage_residual(const Src& r, const SLink& S, int g0c, int gcount,
-                                               float (*sres)[kSlotFloats], Ctx& x, int tid0,
-                                               int nthr) {
-  constexpr int W = 4;
-  const int quads = gcount * 4;
-  for (int q0 = tid0; q0 < quads; q0 += nthr * W) {
-    int e[W];
-#pragma unroll
-    for (int m = 0; m < W; ++m) {
-      const int q = q0 + m * nthr;
-      e[m] = -1;
-      if (q < quads) {
-        const int g = g0c + q / 4;
-        const int row = 16 * g + 4 * (q & 3);
-        int clo, chi;
-        group_owners(S, g, x.C, clo, chi);
-        if (clo == static_cast<int>(x.c) && row < S.n) e[m] = row;
-      }
-    }
-    const Src R1[1] = {r};
-    float4 v[1][W];
-    if (!gather<W, 1>(R1, x, e, v)) return false;
-#pragma unroll
-    for (int m = 0; m < W; ++m) {
-      if (e[m] < 0) continue;
-      const int q = q0 + m * nthr;
-      *reinterpret_cast<float4*>(&sres[q / 4][4 * (q & 3)]) = v[0][m];
-    }
-  }
-  return true;
 }
 
 // Argmax candidates: larger value wins, then the lower index; NaN never wins.
@@ -374,8 +390,10 @@ __device__ __forceinline__ void warp_best(float& bv, int& bi) {
   }
 }
 
-// A warp's weight stream: its tiles of every link in order, kStages in flight
-// through its ring.  `left` tiles remain in link ps, the next one at psrc.
+// A warp's weight stream: its tiles of every link in order, in chunks of up to
+// kChunk tiles (a warp range is cut into chunks from its start), kSlots chunks
+// in flight through its ring.  `left` tiles remain in link ps, the next one at
+// psrc.
 struct TileStream {
   int ps, left, issued, consumed;
   const uint8_t* psrc;
@@ -399,59 +417,65 @@ __device__ __forceinline__ void stream_issue(const SLink* sl, int n_links, TileS
                                              int warp, int lane, uint32_t ring, uint32_t bar0,
                                              uint64_t pol) {
   if (ts.ps >= n_links) return;
+  const int nt = ts.left < kChunk ? ts.left : kChunk;
   if (lane == 0) {
-    const uint32_t slot = static_cast<uint32_t>(ts.issued) & (kStages - 1);
-    mbar_arrive_expect_tx(bar0 + 8 * slot, rt::kTileBytes);
-    bulk_g2s(ring + slot * rt::kTileBytes, ts.psrc, rt::kTileBytes, bar0 + 8 * slot, pol);
+    const uint32_t slot = static_cast<uint32_t>(ts.issued) & (kSlots - 1);
+    mbar_arrive_expect_tx(bar0 + 8 * slot, nt * rt::kTileBytes);
+    bulk_g2s(ring + slot * kChunkBytes, ts.psrc, nt * rt::kTileBytes, bar0 + 8 * slot, pol);
   }
   ++ts.issued;
-  ts.psrc += rt::kTileBytes;
-  if (--ts.left == 0) stream_settle(sl, n_links, ts, warp);
+  ts.psrc += nt * rt::kTileBytes;
+  ts.left -= nt;
+  if (ts.left == 0) stream_settle(sl, n_links, ts, warp);
 }
 
-// This warp's tiles [wa, wb) of the current link: each 16-row group's row
-// products end in Pw[group - first group][row].  Kept out of line so that the
-// decode loop is register-allocated on its own.
-__device__ __forceinline__ bool run_tiles(const SLink* sl, int n_links, TileStream& tsr, Ctx& x,
-                                       int warp, int lane, uint32_t ring, uint32_t bar0,
-                                       uint32_t xs_addr, int wa, int wb, int nsb,
-                                       float (*Pw)[kSlotFloats]) {
+// This warp's tiles [wa, wb) of the current link (g0w = wa / nsb): each
+// 16-row group's row products end in Pw[group - g0w][row].  Kept out of line
+// so that the decode loop is register-allocated on its own (inlined, the
+// staging code's live values cost it spills).
+__device__ __noinline__ bool run_tiles(const SLink* sl, int n_links, TileStream& tsr, Ctx& x,
+                                          int warp, int lane, const uint8_t* ring_p,
+                                          uint32_t ring, uint32_t bar0, const uint8_t* x16,
+                                          const float* xinv, int wa, int wb, int g0w, int nsb,
+                                          float (*Pw)[kSlotFloats]) {
   TileStream ts = tsr;
   const uint64_t pol = l2_evict_first_policy();
-  const rt::PairConsts pc = rt::make_pair_consts();
-  const int g0w = wa < wb ? wa / nsb : 0;
   int cur = -1;
-  float yv[4] = {0.f, 0.f, 0.f, 0.f};
+  float y[2] = {0.f, 0.f};
   auto flush = [&](int g) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      float v = yv[j];
-      v += __shfl_xor_sync(0xffffffffu, v, 1);
-      v += __shfl_xor_sync(0xffffffffu, v, 2);
-      v += __shfl_xor_sync(0xffffffffu, v, 4);
-      if ((lane & 7) == 0) Pw[g - g0w][4 * (lane >> 3) + j] = v;
-      yv[j] = 0.f;
+    if ((lane & 3) == 0) {
+      Pw[g - g0w][lane >> 2] = y[0];
+      Pw[g - g0w][(lane >> 2) + 8] = y[1];
     }
+    y[0] = y[1] = 0.f;
   };
   bool ok = true;
   int g = g0w, t = wa - g0w * nsb;
-  for (int i = wa; i < wb; ++i) {
-    const uint32_t slot = static_cast<uint32_t>(ts.consumed) & (kStages - 1);
-    const uint32_t parity = static_cast<uint32_t>(ts.consumed / kStages) & 1u;
+  for (int i = wa; i < wb; i += kChunk) {
+    const int nt = wb - i < kChunk ? wb - i : kChunk;
+    const uint32_t slot = static_cast<uint32_t>(ts.consumed) & (kSlots - 1);
+    const uint32_t parity = static_cast<uint32_t>(ts.consumed / kSlots) & 1u;
     const bool landed = mbar_wait(bar0 + 8 * slot, parity, x.s_abort);
     if (!__all_sync(0xffffffffu, landed)) {
       if (lane == 0) fail(x);
       ok = false;
       break;
     }
-    if (g != cur) {
-      if (cur >= 0) flush(cur);
-      cur = g;
-    }
-    rt::tile_dot(ring + slot * rt::kTileBytes, xs_addr, t, lane, pc, yv);
-    if (++t == nsb) {
-      t = 0;
-      ++g;
+    const uint8_t* chunk = ring_p + slot * kChunkBytes;
+#pragma unroll
+    for (int p = 0; p < kChunk; ++p) {
+      if (p < nt) {
+        if (g != cur) {
+          if (cur >= 0) flush(cur);
+          cur = g;
+        }
+        rt::tile_dot(chunk + p * rt::kTileBytes, x16 + t * (16 * rt::kXStepBytes), xinv + 8 * t,
+                     lane, y);
+        if (++t == nsb) {
+          t = 0;
+          ++g;
+        }
+      }
     }
     __syncwarp();
     fence_proxy_async_smem();
@@ -463,35 +487,15 @@ __device__ __forceinline__ bool run_tiles(const SLink* sl, int n_links, TileStre
   return ok;
 }
 
-__device__ __forceinline__ Src make_src(const ChainArgs& A, const SLink* sl, int s, int j) {
-  const ChainLink& L = A.L[s];
-  Src r;
-  const int t = L.src_link[j];
-  r.off = L.src_off[j];
-  r.ext = L.ext[j];
-  r.slots = nullptr;
-  r.nsb = 1;
-  r.unit = 1;
-  r.shift = 4;
-  r.divU = Div{0, 0, 1};
-  if (t >= 0) {
-    r.slots = sl[t].slots;
-    r.nsb = sl[t].nsb;
-    r.unit = sl[t].unit;
-    r.shift = (sl[t].ops & kOpSwiglu) ? 3 : 4;
-    r.divU = sl[t].divU;
-  }
-  return r;
-}
-
 __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constant__ ChainArgs A) {
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ __align__(8) uint64_t full_bar[kWarps][kStages];
+  __shared__ __align__(8) uint64_t full_bar[kWarps][kSlots];
   __shared__ __align__(8) uint64_t never_bar;
   __shared__ __align__(16) float P[kWarps][kWarpGroups][kSlotFloats];
   __shared__ __align__(16) float sres[kCtaGroups][kSlotFloats];
   __shared__ __align__(16) SLink s_links[kMaxLinks];
   __shared__ int s_wa[kWarps], s_wb[kWarps];
+  __shared__ int2 s_wg[kWarps];  // first and last group of each warp range (empty: 1, 0)
   __shared__ float sown[kSlotFloats];
   __shared__ float s_bv[kWarps];
   __shared__ int s_bi[kWarps];
@@ -505,31 +509,41 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
   x.hdr = A.hdr;
   x.status = A.status;
   const int n_links = A.n_links;
-  float* xs = reinterpret_cast<float*>(smem);
-  const uint32_t xs_addr = smem_u32(smem);
-  const uint32_t xs_bytes = static_cast<uint32_t>((rt::xpad_floats(A.kmax) * 4 + 127) / 128 * 128);
-  const uint32_t ring = xs_addr + xs_bytes + warp * kStages * rt::kTileBytes;
+  // dynamic shared memory: ring | staged x | inverse block scales
+  uint8_t* const ring_p = smem + warp * kSlots * kChunkBytes;
+  const uint32_t ring = smem_u32(ring_p);
+  uint8_t* const x16 = smem + kWarps * kSlots * kChunkBytes;
+  float* const xinv = reinterpret_cast<float*>(x16 + rt::x16_bytes(A.kmax));
   const uint32_t bar0 = smem_u32(&full_bar[warp][0]);
   const uint64_t pol = l2_evict_first_policy();
 
   // the header's words are loaded together, first, so that their latency
-  // overlaps the set-up below
+  // overlaps the set-up and the first weight copies below (nothing before the
+  // slot-set reset depends on them)
   const uint32_t epoch = ld_relaxed_u32(A.hdr + kHdrEpoch);
   const uint32_t clean0 = ld_relaxed_u32(A.hdr + kHdrClean0);
   const uint32_t clean1 = ld_relaxed_u32(A.hdr + kHdrClean1);
-  const int set = static_cast<int>(epoch & 1u);
   if (tid == 0) {
     s_abort = 0;
     mbar_init(smem_u32(&never_bar), 1);
   }
   if (lane == 0)
-    for (int i = 0; i < kStages; ++i) mbar_init(bar0 + 8 * i, 1);
+    for (int i = 0; i < kSlots; ++i) mbar_init(bar0 + 8 * i, 1);
   for (int s = tid; s < n_links; s += kThreads) {
     const ChainLink& L = A.L[s];
     SLink& S = s_links[s];
     const uint32_t units = static_cast<uint32_t>(L.tiles / L.unit);
     S.R = L.R;
-    S.slots = A.set[set] + static_cast<size_t>(L.slot0) * kSlotFloats;
+    S.y = L.y;
+    S.argmax = L.argmax;
+    for (int j = 0; j < 2; ++j) {
+      S.ext[j] = L.ext[j];
+      S.src_link[j] = L.src_link[j];
+      S.src_off[j] = L.src_off[j];
+    }
+    S.k = L.k;
+    S.rec0 = L.rec0;
+    S.slot0 = L.slot0;
     S.ca = L.unit * static_cast<int>(divq(units * x.c, A.divC));
     S.cb = L.unit * static_cast<int>(divq(units * (x.c + 1), A.divC));
     S.nsb = L.nsb;
@@ -537,25 +551,32 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
     S.unit = L.unit;
     S.units = static_cast<int>(units);
     S.divU = L.divU;
+    S.divNsb = L.divNsb;
     S.ops = L.ops;
+    S.g0c = static_cast<int>(divq(static_cast<uint32_t>(S.ca), L.divNsb));
+    S.gcount = S.ca < S.cb
+                   ? static_cast<int>(divq(static_cast<uint32_t>(S.cb - 1), L.divNsb)) - S.g0c + 1
+                   : 0;
   }
   fence_mbarrier_init();
   __syncthreads();
-  const uint32_t clean_mine = set ? clean1 : clean0;
 
-  // ---- this warp's weight stream: the first kStages tiles go out now
+  // ---- this warp's weight stream: the first kSlots chunks go out now
   TileStream ts;
   ts.ps = 0;
   ts.issued = 0;
   ts.consumed = 0;
   stream_enter(s_links, ts, warp);
   stream_settle(s_links, n_links, ts, warp);
-  for (int i = 0; i < kStages; ++i)
+  for (int i = 0; i < kSlots; ++i)
     stream_issue(s_links, n_links, ts, warp, lane, ring, bar0, pol);
 
   // ---- slot sets: a fresh workspace (or one last used with a smaller chain)
   // gets both sets reset before anyone publishes; otherwise the set of the
   // next launch is reset while this one runs.
+  const int set = static_cast<int>(epoch & 1u);
+  const uint32_t clean_mine = set ? clean1 : clean0;
+  float* const set_base = A.set[set];
   {
     const bool fresh = epoch == 0u || clean_mine < A.set_floats;
     const uint32_t total = A.set_floats / 4;  // float4s per set
@@ -589,40 +610,78 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
   // Every decision taken on the abort flag is made uniform by a barrier that
   // ORs it over the CTA, so that no warp or CTA splits around a collective.
   volatile int* abort_flag = &s_abort;
-  bool stop = false;
+  bool stop = __syncthreads_or(*abort_flag) != 0;
 
-  for (int s = 0; s <= n_links; ++s) {
+  for (int s = 0; s <= n_links && !stop; ++s) {
+    const bool last = s == n_links;
+    // ---------------- before waiting on other CTAs: this link's warp ranges
+    // and the addresses of everything it reads
+    bool finish_prev = false;  // this CTA first-owns a split group of link s-1
+    if (s > 0) {
+      const SLink& S1 = s_links[s - 1];
+      if (S1.gcount > 0 && (S1.y != nullptr || (S1.ops & kOpArgmax))) {
+        const int g = S1.g0c + S1.gcount - 1;
+        finish_prev = g * S1.nsb >= S1.ca && (g + 1) * S1.nsb > S1.cb;
+      }
+    }
+    int need = finish_prev ? s - 1 : -1;
+    Ent en[kStageQuads + 1];  // x quads of the first staging pass, then a residual quad
+#pragma unroll
+    for (int m = 0; m <= kStageQuads; ++m) en[m].np = -1;
+    if (!last) {
+      const SLink& S = s_links[s];
+      need = max(need, S.src_link[0]);
+      if (S.ops & kOpResidual) need = max(need, S.src_link[1]);
+      if (lane == 0) {
+        int a, b;
+        warp_range(S.ca, S.cb, warp, a, b);
+        s_wa[warp] = a;
+        s_wb[warp] = b;
+        s_wg[warp] = a < b ? make_int2(static_cast<int>(divq(static_cast<uint32_t>(a), S.divNsb)),
+                                       static_cast<int>(divq(static_cast<uint32_t>(b - 1), S.divNsb)))
+                           : make_int2(1, 0);
+      }
+      if (S.gcount > 0) {
+        x_entries(s_links, set_base, S, 0, tid, x.C, en);
+        // the residual rows of the groups this CTA holds the first tile of
+        if ((S.ops & kOpResidual) && tid < S.gcount * 4) {
+          const int g = S.g0c + tid / 4, row = 16 * g + 4 * (tid & 3);
+          if (g * S.nsb >= S.ca && row < S.n)
+            en[kStageQuads] = make_entry(s_links, set_base, S.ext[1], S.src_link[1],
+                                         S.src_off[1] + row, x.C);
+        }
+      }
+    }
+    wait_link_done(x, need, tid);
+
     // ---------------- finish link s-1: the CTA's split first-owned group
-    if (s > 0 && warp == kWarps - 1 && !stop) {
-      const ChainLink& P1 = A.L[s - 1];
+    if (s > 0 && warp == kWarps - 1) {
       const SLink& S1 = s_links[s - 1];
       float fv = 0.f;
       int fi = -1;
-      if (S1.ca < S1.cb && (P1.y != nullptr || (S1.ops & kOpArgmax))) {
-        const int g = (S1.cb - 1) / S1.nsb;
+      if (finish_prev && lane < kSlotFloats) {
+        const int g = S1.g0c + S1.gcount - 1;
         int clo, chi;
         group_owners(S1, g, x.C, clo, chi);
-        if (clo == static_cast<int>(x.c) && chi > clo && lane < kSlotFloats) {
-          float v = sown[lane];
-          bool ok = true;
-          for (int cc = clo + 1; cc <= chi && ok; ++cc) {
-            const uint32_t* q = reinterpret_cast<const uint32_t*>(
-                S1.slots + static_cast<size_t>(g + cc) * kSlotFloats + lane);
-            x.t0 = global_timer_ns();
-            int sp = 0;
-            uint32_t u;
-            while ((u = ld_relaxed_u32(q)) == kEmpty)
-              if (!keep_waiting(x, sp)) {
-                ok = false;
-                break;
-              }
-            v += __uint_as_float(u);
-          }
-          const int row = 16 * g + lane;
-          if (ok && row < S1.n) {
-            if (P1.y != nullptr) P1.y[row] = v;
-            better(fv, fi, v, row);
-          }
+        float v = sown[lane];
+        bool ok = true;
+        for (int cc = clo + 1; cc <= chi && ok; ++cc) {
+          const uint32_t* q = reinterpret_cast<const uint32_t*>(
+              set_base + static_cast<size_t>(S1.slot0 + g + cc) * kSlotFloats + lane);
+          x.t0 = global_timer_ns();
+          int sp = 0;
+          uint32_t u;
+          while ((u = ld_relaxed_u32(q)) == kEmpty)
+            if (!keep_waiting(x, sp)) {
+              ok = false;
+              break;
+            }
+          v += __uint_as_float(u);
+        }
+        const int row = 16 * g + lane;
+        if (ok && row < S1.n) {
+          if (S1.y != nullptr) S1.y[row] = v;
+          better(fv, fi, v, row);
         }
       }
       if (S1.ops & kOpArgmax) {
@@ -634,37 +693,38 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
           int i = fi;
           for (int w = 0; w < kWarps; ++w)
             if (s_bi[w] >= 0) better(v, i, s_bv[w], s_bi[w]);
-          float* rec = A.set[set] + P1.rec0 + 2 * x.c;
+          float* rec = set_base + S1.rec0 + 2 * x.c;
           st_relaxed_f32(rec, i >= 0 ? v : 0.f);
           st_relaxed_f32(rec + 1, __int_as_float(i));
         }
       }
     }
-    if (s == n_links) break;
+    if (last) break;
     const SLink& S = s_links[s];
-    const int ca = S.ca, cb = S.cb;
-    const int g0c = ca < cb ? ca / S.nsb : 0;
-    const int gcount = ca < cb ? (cb - 1) / S.nsb - g0c + 1 : 0;
-    if (lane == 0) {
-      int a, b;
-      warp_range(ca, cb, warp, a, b);
-      s_wa[warp] = a;
-      s_wb[warp] = b;
-    }
+    const int ca = S.ca, cb = S.cb, g0c = S.g0c, gcount = S.gcount;
 
     // ---------------- stage x_s (and the residual rows this CTA adds)
-    if (!*abort_flag && ca < cb) {
-      // every thread keeps up to 9 element quads in flight: one pass for k <= 9216
-      const bool ok = stage_x<9>(make_src(A, s_links, s, 0), A.L[s].k, xs, x, tid, kThreads);
-      if (ok && (S.ops & kOpResidual) && gcount > 0)
-        stage_residual(make_src(A, s_links, s, 1), S, g0c, gcount, sres, x, tid, kThreads);
+    if (!*abort_flag && gcount > 0) {
+      float4 v[kStageQuads + 1];
+      bool ok = load_entries(en, x, v);
+      if (ok) {
+        convert_x(v, en, 0, tid, x16, xinv);
+        if (en[kStageQuads].np >= 0)
+          *reinterpret_cast<float4*>(&sres[tid / 4][4 * (tid & 3)]) = v[kStageQuads];
+      }
+      for (int pass = 1; ok && pass * kStageQuads * kThreads < S.k / 4; ++pass) {
+        x_entries(s_links, set_base, S, pass, tid, x.C, en);
+        en[kStageQuads].np = -1;
+        ok = load_entries(en, x, v);
+        if (ok) convert_x(v, en, pass, tid, x16, xinv);
+      }
     }
     stop = __syncthreads_or(*abort_flag) != 0;
     if (stop) break;
 
     // ---------------- this warp's tiles of link s
-    run_tiles(s_links, n_links, ts, x, warp, lane, ring, bar0, xs_addr, s_wa[warp], s_wb[warp],
-              S.nsb, P[warp]);
+    run_tiles(s_links, n_links, ts, x, warp, lane, ring_p, ring, bar0, x16, xinv, s_wa[warp],
+              s_wb[warp], s_wg[warp].x, S.nsb, P[warp]);
     stop = __syncthreads_or(*abort_flag) != 0;
     if (stop) break;
 
@@ -676,51 +736,51 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
       // ca / nsb when the link has fewer tiles than SMs; readers of that group
       // count it among the group's CTAs, so it publishes zeros there.  Its
       // slot index ca / nsb + c is still unique.
-      st_relaxed_f32(S.slots + static_cast<size_t>(ca / S.nsb + x.c) * kSlotFloats + tid, 0.f);
+      st_relaxed_f32(set_base + static_cast<size_t>(S.slot0 + g0c + x.c) * kSlotFloats + tid,
+                     0.f);
     }
     if (gcount > 0 && (S.ops & kOpSwiglu)) {
       // gated link (whole groups): 8 values per group, a * sigmoid(a) * b
-      float* const y = A.L[s].y;
+      float* const y = S.y;
       for (int idx = tid; idx < gcount * 8; idx += kThreads) {
         const int gl = idx >> 3, j = idx & 7, g = g0c + gl;
-        const int t0 = g * S.nsb, t1 = t0 + S.nsb;
         float a = 0.f, b = 0.f;
+#pragma unroll
         for (int w = 0; w < kWarps; ++w) {
-          const int wa = s_wa[w], wb = s_wb[w];
-          if (wa < wb && wa < t1 && wb > t0) {
-            a += P[w][g - wa / S.nsb][j];
-            b += P[w][g - wa / S.nsb][j + 8];
+          const int2 r = s_wg[w];
+          if (g >= r.x && g <= r.y) {
+            a += P[w][g - r.x][j];
+            b += P[w][g - r.x][j + 8];
           }
         }
         const float v = silu_gate(a, b);
-        st_relaxed_f32(S.slots + static_cast<size_t>(g + x.c) * kSlotFloats + j, v);
+        st_relaxed_f32(set_base + static_cast<size_t>(S.slot0 + g + x.c) * kSlotFloats + j, v);
         if (y != nullptr && 8 * g + j < S.n / 2) y[8 * g + j] = v;
       }
     } else if (gcount > 0) {
-      float* const y = A.L[s].y;
+      float* const y = S.y;
       for (int idx = tid; idx < gcount * kSlotFloats; idx += kThreads) {
         const int gl = idx >> 4, row16 = idx & 15, g = g0c + gl;
-        const int t0 = g * S.nsb, t1 = t0 + S.nsb;
         float sum = 0.f;
+#pragma unroll
         for (int w = 0; w < kWarps; ++w) {
-          const int a = s_wa[w], b = s_wb[w];
-          if (a < b && a < t1 && b > t0) sum += P[w][g - a / S.nsb][row16];
+          const int2 r = s_wg[w];
+          if (g >= r.x && g <= r.y) sum += P[w][g - r.x][row16];
         }
-        int clo, chi;
-        group_owners(S, g, x.C, clo, chi);
-        const bool first = clo == static_cast<int>(x.c);
+        // this CTA holds the group's first tile / all of its tiles
+        const bool first = g * S.nsb >= ca;
+        const bool whole = first && (g + 1) * S.nsb <= cb;
         if (first && (S.ops & kOpResidual)) sum += sres[gl][row16];
-        st_relaxed_f32(S.slots + static_cast<size_t>(g + x.c) * kSlotFloats + row16, sum);
+        st_relaxed_f32(set_base + static_cast<size_t>(S.slot0 + g + x.c) * kSlotFloats + row16,
+                       sum);
         const int row = 16 * g + row16;
-        if (first) {
-          if (chi == clo) {
-            if (row < S.n) {
-              if (y != nullptr) y[row] = sum;
-              better(bv, bi, sum, row);
-            }
-          } else {
-            sown[row16] = sum;
+        if (whole) {
+          if (row < S.n) {
+            if (y != nullptr) y[row] = sum;
+            better(bv, bi, sum, row);
           }
+        } else if (first) {
+          sown[row16] = sum;
         }
       }
     }
@@ -732,16 +792,18 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
       }
     }
     stop = __syncthreads_or(*abort_flag) != 0;
-    if (stop) break;
+    // this CTA is done with link s: its slot stores are issued (the readers
+    // check the values, the count only tells them when to look)
+    if (!stop && tid == 0) red_relaxed_add(A.hdr + kHdrCount + s, 1u);
   }
 
   // ---------------- argmax over the CTAs' records (CTA 0), then the epoch
   stop = __syncthreads_or(*abort_flag) != 0;
   if (!stop && x.c == 0 && warp == 0) {
     for (int s = 0; s < n_links; ++s) {
-      const ChainLink& L = A.L[s];
+      const SLink& L = s_links[s];
       if (!(L.ops & kOpArgmax)) continue;
-      const uint32_t* rec = reinterpret_cast<const uint32_t*>(A.set[set] + L.rec0);
+      const uint32_t* rec = reinterpret_cast<const uint32_t*>(set_base + L.rec0);
       float v = 0.f;
       int i = -1;
       bool ok = true;
@@ -771,10 +833,12 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
   }
   __syncthreads();
   if (tid == 0 && !*abort_flag) {
-    // the last CTA to finish records that the next set is clean and moves the epoch
+    // the last CTA to finish records that the next set is clean, puts the
+    // link counters back to zero and moves the epoch
     const uint32_t prev = atomicAdd(A.hdr + kHdrFinished, 1u);
     if (prev == x.C - 1) {
       // every other CTA is done with the header: plain stores, nothing waits
+      for (int s = 0; s < n_links; ++s) st_relaxed_u32(A.hdr + kHdrCount + s, 0u);
       st_relaxed_u32(A.hdr + kHdrFinished, 0u);
       st_relaxed_u32(A.hdr + kHdrBarrier, 0u);
       st_relaxed_u32(A.hdr + (set ? kHdrClean0 : kHdrClean1), A.set_floats);
@@ -783,51 +847,57 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
   }
   // copies this warp still has in flight land before the CTA exits
   for (int q = ts.consumed; q < ts.issued; ++q)
-    mbar_wait(bar0 + 8 * static_cast<uint32_t>(q % kStages),
-              static_cast<uint32_t>((q / kStages) & 1));
+    mbar_wait(bar0 + 8 * static_cast<uint32_t>(q % kSlots),
+              static_cast<uint32_t>((q / kSlots) & 1));
 }
 
 // ------------------------------------------------------------------ repack
-// Thread per (row, block) of the padded matrix: GGUF block -> repacked tile.
+// Thread per (tile, lane L = 4g + t, step quad j): the lane's 16 code bytes of
+// steps 4j..4j+3 (rows 16G + g and 16G + g + 8, blocks 2j and 2j + 1 of the
+// slice), and for t < 2 the scale word of block 2j + t of both rows.
 __global__ void __launch_bounds__(256) repack_kernel(const uint8_t* __restrict__ W, int64_t n,
                                                      int64_t k, uint8_t* __restrict__ R) {
-  const int64_t nb = k / 32, rows = (n + 15) / 16 * 16;
+  const int64_t nb = k / 32, nsb = k / 256, tiles = (n + 15) / 16 * nsb;
   const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (idx >= rows * nb) return;
-  const int64_t r = idx / nb, kb = idx - r * nb;
-  const int64_t g = r / 16, t = kb / 8;
-  const int h = static_cast<int>((r & 15) >> 2), j = static_cast<int>(r & 3);
-  const int b = static_cast<int>(kb & 7), L = 8 * h + b;
-  uint8_t* tile = R + (g * (k / 256) + t) * rt::kTileBytes;
-  uint32_t dbits = 0;
-  uint32_t q[16];
-  if (r < n) {
-    const uint8_t* blk = W + (r * nb + kb) * kBlockBytes;
-    dbits = blk[0] | (static_cast<uint32_t>(blk[1]) << 8);
-    uint8_t qs[16];
+  if (idx >= tiles * 128) return;
+  const int64_t tile = idx >> 7;
+  const int L = static_cast<int>(idx & 31), j = static_cast<int>((idx >> 5) & 3);
+  const int g = L >> 2, tq = L & 3;
+  const int64_t G = tile / nsb, t = tile - G * nsb;
+  const int64_t r0 = 16 * G + g, r1 = r0 + 8;
+  uint8_t* out = R + tile * rt::kTileBytes;
+  // code of row r, block kb, element e (padding rows: 8)
+  auto code = [&](int64_t r, int64_t kb, int e) -> uint32_t {
+    if (r >= n) return 8u;
+    const uint8_t* blk = W + (r * nb + kb) * kBlockBytes + 2;
+    return e < 16 ? (blk[e] & 0xFu) : (blk[e - 16] >> 4);
+  };
+  uint32_t words[4];
 #pragma unroll
-    for (int c = 0; c < 16; ++c) qs[c] = blk[2 + c];
-    // GGUF: byte c = element c | element c+16 << 4.  Here byte c = 4u + i
-    // (word u) holds element e = 16 (u / 2) + 4i + (u % 2) low and e + 2 high.
+  for (int u = 0; u < 4; ++u) {
+    const int s = 4 * j + u;               // step
+    const int64_t kb = 8 * t + s / 2;      // block of the step
+    const int e0 = 16 * (s & 1) + 2 * tq;  // element of column 2t of the step
+    uint32_t w = 0;
 #pragma unroll
-    for (int c = 0; c < 16; ++c) {
-      const int u = c >> 2, i = c & 3;
-      const int e0 = 16 * (u >> 1) + 4 * i + (u & 1), e1 = e0 + 2;
-      const uint32_t q0 = e0 < 16 ? (qs[e0] & 0xF) : (qs[e0 - 16] >> 4);
-      const uint32_t q1 = e1 < 16 ? (qs[e1] & 0xF) : (qs[e1 - 16] >> 4);
-      q[c] = q0 | (q1 << 4);
+    for (int m = 0; m < 8; ++m) {
+      const int e = e0 + 8 * ((m >> 1) & 1) + (m >> 2);
+      w |= code((m & 1) ? r1 : r0, kb, e) << (4 * m);
     }
-  } else {
-#pragma unroll
-    for (int c = 0; c < 16; ++c) q[c] = 0x88;
+    words[u] = w;
   }
-  *reinterpret_cast<uint16_t*>(tile + 8 * L + 2 * j) = static_cast<uint16_t>(dbits);
-  uint4 v;
-  v.x = q[0] | (q[1] << 8) | (q[2] << 16) | (q[3] << 24);
-  v.y = q[4] | (q[5] << 8) | (q[6] << 16) | (q[7] << 24);
-  v.z = q[8] | (q[9] << 8) | (q[10] << 16) | (q[11] << 24);
-  v.w = q[12] | (q[13] << 8) | (q[14] << 16) | (q[15] << 24);
-  *reinterpret_cast<uint4*>(tile + rt::kScaleBytes + rt::kCodeRowBytes * j + 16 * L) = v;
+  *reinterpret_cast<uint4*>(out + rt::kScaleBytes + rt::kStepBytes * j + 16 * L) =
+      make_uint4(words[0], words[1], words[2], words[3]);
+  if (tq < 2) {
+    const int b = 2 * j + tq;
+    const int64_t kb = 8 * t + b;
+    auto dbits = [&](int64_t r) -> uint32_t {
+      if (r >= n) return 0u;
+      const uint8_t* blk = W + (r * nb + kb) * kBlockBytes;
+      return blk[0] | (static_cast<uint32_t>(blk[1]) << 8);
+    };
+    *reinterpret_cast<uint32_t*>(out + 32 * g + 4 * b) = dbits(r0) | (dbits(r1) << 16);
+  }
 }
 
 // ------------------------------------------------------------------ host side
@@ -900,6 +970,7 @@ q4_status chain_plan(const q4_chain_link* links, int32_t n, ChainArgs* A, size_t
       c.slot0 = slot;
       c.unit = static_cast<int32_t>(unit);
       c.divU = make_div(static_cast<uint32_t>(tiles / unit));
+      c.divNsb = make_div(static_cast<uint32_t>(nsb));
       c.rec0 = 0;
     }
     for (int j = 0; j < 2; ++j) {
@@ -947,8 +1018,8 @@ q4_status chain_plan(const q4_chain_link* links, int32_t n, ChainArgs* A, size_t
 }
 
 size_t chain_smem_bytes(int kmax) {
-  return static_cast<size_t>((rt::xpad_floats(kmax) * 4 + 127) / 128 * 128) +
-         static_cast<size_t>(kWarps) * kStages * rt::kTileBytes;
+  return static_cast<size_t>(kWarps) * kSlots * kChunkBytes +
+         static_cast<size_t>(rt::x16_bytes(kmax)) + static_cast<size_t>(kmax / 32) * 4;
 }
 
 cudaError_t chain_launch(ChainArgs& A, void* workspace, cudaStream_t s) {
@@ -980,7 +1051,7 @@ cudaError_t chain_launch(ChainArgs& A, void* workspace, cudaStream_t s) {
 }
 
 cudaError_t repack_launch(const uint8_t* W, int64_t n, int64_t k, uint8_t* R, cudaStream_t s) {
-  const int64_t work = (n + 15) / 16 * 16 * (k / 32);
+  const int64_t work = (n + 15) / 16 * (k / 256) * 128;  // (tile, lane, step quad)
   const int64_t blocks = (work + 255) / 256;
   if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
   repack_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(W, n, k, R);

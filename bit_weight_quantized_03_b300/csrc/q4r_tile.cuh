@@ -1,34 +1,40 @@
-// q4r_tile.cuh -- the repacked Q4_0 tile and its batch-1 dot product.
+// q4r_tile.cuh -- the repacked Q4_0 tile and its batch-1 tensor-core dot product.
 //
 // GGUF Q4_0 (the weight format of the quantized path in the GeekNews write-up
 // es.news.hada.io/topic?id=26595, "Arquitectura") stores 18-byte blocks: a
 // binary16 scale d and 16 bytes of 4-bit codes, w = (q - 8) * d.  Streaming
-// those blocks row by row leaves every block at an odd 2-byte offset, so a
-// GPU reads them in 4-byte pieces and re-aligns them in registers.  The
-// repacked layout below keeps every byte of the blocks but moves them so that
-// each lane of a warp finds its data in whole 16-byte and 8-byte words:
+// those blocks row by row leaves every block at an odd 2-byte offset and the
+// codes in an order no arithmetic unit wants.  The repacked layout keeps every
+// byte of the blocks but moves them into the operand order of the tensor
+// cores' 16 x 16 (f16) A fragment:
 //
 //   * rows are taken in groups of 16 and k in slices of 256 (8 blocks); the
-//     16 x 256 tile (group g, slice t) is 2304 contiguous bytes at
-//     (g * k/256 + t) * 2304, so a run of tiles is one contiguous byte range;
-//   * lane L = 8h + b (h = 0..3, b = 0..7) owns rows 4h + j (j = 0..3) of
-//     block b of the slice: their four scales are the 8 bytes at 8L
-//     (binary16, little-endian, row 4h + j at 8L + 2j) and row 4h + j's codes
-//     are the 16 bytes at 256 + 512j + 16L;
-//   * those 16 bytes are four little-endian 32-bit words; nibble m of word u
-//     holds element 16 (u / 2) + 2m + (u % 2).  So nibble m of the word pair
-//     (2w, 2w + 1), read as one 64-bit value, holds the adjacent elements
-//     16w + 2m and 16w + 2m + 1: the bit operations that decode a pair act on
-//     a 64-bit register pair directly and their result feeds one packed
-//     fp32x2 subtract and one packed FMA with no moves in between;
+//     16 x 256 tile (G, t) is 2304 contiguous bytes at (G * k/256 + t) * 2304,
+//     so a run of tiles is one contiguous byte range;
+//   * scales (bytes 0..255): the 32-bit word at 32g + 4b holds the binary16 d
+//     of block b of row g (low half) and of row g + 8 (high half);
+//   * codes (bytes 256..2303): the tile's columns form 16 steps of 16; lane
+//     L = 4g + t of step s owns the 32-bit word at 256 + 512 (s/4) + 16L +
+//     4 (s%4).  Its nibble m holds row g + 8 (m & 1) at column
+//     16s + 2t + 8 ((m >> 1) & 1) + (m >> 2), so a lane's four words for steps
+//     4j..4j+3 are one 16-byte load, and a warp's loads are 512 consecutive
+//     bytes;
 //   * rows past n in the last group are padding with d = +0 and codes 8.
 //
-// The eight lanes that share h read the same rows and blocks b = 0..7; the
-// four lanes that share b read the same 32 activations.  x is staged in
-// shared memory with 16 bytes of padding after every 32 floats, so the eight
-// blocks' activations sit in eight different bank quads and a 16-byte load by
-// the whole warp is served in one pass; the warp's code loads are 512
-// consecutive bytes.
+// Decode: with the word w, (w & 0x000F000F) | 0x64006400 is the binary16 pair
+// (1024 + q_a, 1024 + q_b) for the nibbles at bits 0 and 16, and
+// (w & 0x00F000F0) | 0x64006400 is (1024 + 16 q_c, 1024 + 16 q_d) for those at
+// bits 4 and 20; one packed f16 subtract (- 1032), resp. one packed f16 FMA
+// (x 1/16, - 72), turns them into (q - 8) exactly.  The same on w >> 8 gives
+// the other four nibbles.  These four registers are exactly the A fragment of
+// mma.m16n8k16 (rows g and g + 8, columns 2t, 2t+1 and 2t+8, 2t+9).
+//
+// B: the activation x enters the tensor core as binary16, so it is carried as
+// an exact-to-2^-22 pair hi + lo in columns 0 and 1 of B (columns 2..7 are
+// zero), after scaling each 32-element block of x by a power of two that puts
+// its largest magnitude in [2^14, 2^15): rows g / g+8 of the result then sit in
+// the lanes t = 0 as D columns 0 (hi part) and 1 (lo part).  Per block the
+// fp32 fragment sums are multiplied by d and by the block's inverse scale.
 #pragma once
 
 #include "q4_device.cuh"
@@ -39,105 +45,110 @@ namespace rt {
 constexpr int kRows = 16;            // rows per tile
 constexpr int kCols = 256;           // columns (8 blocks) per tile
 constexpr int kTileBytes = 2304;     // 16 rows x 8 blocks x 18 bytes
-constexpr int kScaleBytes = 256;     // 32 lanes x 4 binary16 scales
-constexpr int kCodeRowBytes = 512;   // 32 lanes x 16 bytes, one per row j
+constexpr int kScaleBytes = 256;     // 8 row pairs x 8 blocks x 2 binary16
+constexpr int kStepBytes = 512;      // code bytes of four steps (32 lanes x 16)
+constexpr int kXStepBytes = 64;      // staged x of one 16-column step
 
-// x in shared memory: element e at float index e + 4 * (e / 32).
-__host__ __device__ constexpr int64_t xpad_floats(int64_t k) { return k + k / 32 * 4; }
-__device__ __forceinline__ int xpad(int e) { return e + ((e >> 5) << 2); }
-
-// Decode constants, each in both halves of a 64-bit value: the exponent bits
-// of 2^(23 - p) for p = 0, 4, 8, 12, 16 (a nibble at bit p OR-ed with them
-// reads as the float 2^(23-p) + q) and the bias 2^(23-p) + 8.  Written through
-// an opaque move so that the OR takes them from registers.
-struct PairConsts {
-  unsigned long long bits[5];
-  unsigned long long bias[5];
-};
-
-__device__ __forceinline__ PairConsts make_pair_consts() {
-  PairConsts c;
-  const uint32_t b[5] = {NibbleMagic<0>::kBits, NibbleMagic<4>::kBits, NibbleMagic<8>::kBits,
-                         NibbleMagic<12>::kBits, NibbleMagic<16>::kBits};
-  const float f[5] = {NibbleMagic<0>::kBias, NibbleMagic<4>::kBias, NibbleMagic<8>::kBias,
-                      NibbleMagic<12>::kBias, NibbleMagic<16>::kBias};
-#pragma unroll
-  for (int i = 0; i < 5; ++i) {
-    const uint32_t bb = opaque(b[i]), fb = opaque(__float_as_uint(f[i]));
-    c.bits[i] = (static_cast<unsigned long long>(bb) << 32) | bb;
-    c.bias[i] = (static_cast<unsigned long long>(fb) << 32) | fb;
-  }
-  return c;
+// Staged x: per step s, 64 bytes: for column n = 0 (hi) / 1 (lo) and lane
+// quad t, two words {x[16s+2t], x[16s+2t+1]} and {x[16s+2t+8], x[16s+2t+9]}
+// (binary16 pairs, lower column in the low half) at s*64 + (4n + t)*8.  So the
+// eight lanes 0..7 of a warp fetch their B fragment of a step with one 8-byte
+// load each at s*64 + lane*8.
+__host__ __device__ constexpr int64_t x16_bytes(int64_t k) { return k / 16 * kXStepBytes; }
+// Byte offset of the word holding column pair (i, i+1) (i even) of step s in
+// column n.
+__device__ __forceinline__ int x16_word(int s, int n, int i) {
+  return s * kXStepBytes + (4 * n + ((i & 7) >> 1)) * 8 + ((i >> 3) << 2);
 }
 
-// (q - 8) of the nibbles at bit P of both halves of v, exact, as an fp32 pair:
-// a 64-bit AND and OR (one LOP3 per half) and one packed subtract.
-template <int P>
-__device__ __forceinline__ unsigned long long qm8_pair(unsigned long long v, unsigned long long bits,
-                                                       unsigned long long bias) {
-  static_assert(P >= 0 && P <= 16 && P % 4 == 0, "nibble must sit in the significand");
-  constexpr unsigned long long kMask = static_cast<unsigned long long>(0xFu << P) * 0x100000001ull;
-  unsigned long long r;
-  asm("{\n\t"
-      "and.b64 %0, %1, %2;\n\t"
-      "or.b64 %0, %0, %3;\n\t"
-      "sub.rn.f32x2 %0, %0, %4;\n\t}"
-      : "=l"(r)
-      : "l"(v), "n"(kMask), "l"(bits), "l"(bias));
+// Power-of-two scale for a block whose largest magnitude is amax: s puts amax
+// in [2^14, 2^15) (clamped to 2^-126 .. 2^126); returns s and 1/s, both exact.
+__device__ __forceinline__ void block_scale(float amax, float& s, float& inv) {
+  const int ef = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFF);
+  int se = 268 - ef;  // biased exponent of 2^(14 - (ef - 127))
+  se = amax == 0.f ? 127 : (se < 1 ? 1 : (se > 253 ? 253 : se));
+  s = __uint_as_float(static_cast<uint32_t>(se) << 23);
+  inv = __uint_as_float(static_cast<uint32_t>(254 - se) << 23);
+}
+
+// hi + lo of v (already scaled): hi = f16(v), lo = f16(v - hi).
+__device__ __forceinline__ void split_hi_lo(float v, __half& hi, __half& lo) {
+  hi = __float2half_rn(v);
+  lo = __float2half_rn(v - __half2float(hi));
+}
+
+__device__ __forceinline__ uint32_t lop3_magic(uint32_t w, uint32_t mask) {
+  uint32_t r;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(w), "r"(mask), "r"(0x64006400u));
   return r;
 }
 
-// sum over the 16 elements of word pair v (its nibble m = elements 2m, 2m+1 of
-// the half-block) of (q - 8) * x, accumulated into acc as an fp32 pair; xb[m]
-// holds the activation pair of nibble m.  Nibbles 5..7 (bits 20..31 of each
-// word) are read after one 64-bit shift by 12, which moves each word's top
-// three nibbles to bits 8..19 (bits shifted in from the high word land above
-// bit 19 and are masked off).
-__device__ __forceinline__ unsigned long long pair_dot(unsigned long long v,
-                                                       const unsigned long long* xb,
-                                                       const PairConsts& c, unsigned long long acc,
-                                                       bool first) {
-  const unsigned long long t = v >> 12;
-  const unsigned long long a0 = qm8_pair<0>(v, c.bits[0], c.bias[0]);
-  acc = first ? fmul2(a0, xb[0]) : ffma2(a0, xb[0], acc);
-  acc = ffma2(qm8_pair<4>(v, c.bits[1], c.bias[1]), xb[1], acc);
-  acc = ffma2(qm8_pair<8>(v, c.bits[2], c.bias[2]), xb[2], acc);
-  acc = ffma2(qm8_pair<12>(v, c.bits[3], c.bias[3]), xb[3], acc);
-  acc = ffma2(qm8_pair<16>(v, c.bits[4], c.bias[4]), xb[4], acc);
-  acc = ffma2(qm8_pair<8>(t, c.bits[2], c.bias[2]), xb[5], acc);
-  acc = ffma2(qm8_pair<12>(t, c.bits[3], c.bias[3]), xb[6], acc);
-  acc = ffma2(qm8_pair<16>(t, c.bits[4], c.bias[4]), xb[7], acc);
-  return acc;
+__device__ __forceinline__ uint32_t h2_bits(__half2 h) {
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ __half2 bits_h2(uint32_t u) {
+  return *reinterpret_cast<__half2*>(&u);
 }
 
-// One tile for this lane: yv[j] += d_j * sum_e (q_je - 8) x_e over block b of
-// rows 4h + j.  tile = shared address of the landed tile, xs = shared address
-// of the padded x, t = the tile's slice of k.
-__device__ __forceinline__ void tile_dot(uint32_t tile, uint32_t xs, int t, int lane,
-                                         const PairConsts& c, float (&yv)[4]) {
-  const int b = lane & 7;
-  unsigned long long xb[16];
-  const uint32_t xa = xs + 4 * xpad(t * kCols + 32 * b);
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    asm volatile("ld.shared.v2.b64 {%0, %1}, [%2];"
-                 : "=l"(xb[2 * i]), "=l"(xb[2 * i + 1])
-                 : "r"(xa + 16 * i));
-  }
-  uint32_t s01, s23;
-  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(s01), "=r"(s23) : "r"(tile + 8 * lane));
-  const float d[4] = {half_bits_to_float(s01), half_bits_to_float(s01 >> 16),
-                      half_bits_to_float(s23), half_bits_to_float(s23 >> 16)};
+// D (+)= A B for one m16n8k16 step, f16 operands, fp32 accumulate.
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                        uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// The A fragment (q - 8 as f16) of one step word.
+__device__ __forceinline__ void decode_step(uint32_t w, uint32_t (&a)[4]) {
+  const __half2 k1032 = __half2half2(__ushort_as_half(0x6408));   // 1032
+  const __half2 k16 = __half2half2(__ushort_as_half(0x2C00));     // 1/16
+  const __half2 km72 = __half2half2(__ushort_as_half(0xD480));    // -72
+  const uint32_t t = w >> 8;
+  a[0] = h2_bits(__hsub2(bits_h2(lop3_magic(w, 0x000F000Fu)), k1032));
+  a[1] = h2_bits(__hfma2(bits_h2(lop3_magic(w, 0x00F000F0u)), k16, km72));
+  a[2] = h2_bits(__hsub2(bits_h2(lop3_magic(t, 0x000F000Fu)), k1032));
+  a[3] = h2_bits(__hfma2(bits_h2(lop3_magic(t, 0x00F000F0u)), k16, km72));
+}
+
+// One tile for this warp: y[0] += row g's and y[1] += row g+8's dot product
+// with the tile's 256 columns of x (meaningful in lanes with lane % 4 == 0;
+// the other lanes accumulate zeros).  tile: the landed tile; xs: the staged x
+// of the tile's slice (16 steps); xinv: the slice's 8 inverse block scales.
+__device__ __forceinline__ void tile_dot(const uint8_t* tile, const uint8_t* xs,
+                                         const float* xinv, int lane, float (&y)[2]) {
+  const int g = lane >> 2;
+  const bool bl = lane < 8;  // lanes that carry B columns 0 and 1
+  const uint4 sa = *reinterpret_cast<const uint4*>(tile + 32 * g);
+  const uint4 sb = *reinterpret_cast<const uint4*>(tile + 32 * g + 16);
+  const float4 fa = *reinterpret_cast<const float4*>(xinv);
+  const float4 fb = *reinterpret_cast<const float4*>(xinv + 4);
+  const uint32_t sw[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
+  const float f[8] = {fa.x, fa.y, fa.z, fa.w, fb.x, fb.y, fb.z, fb.w};
+  const uint8_t* codes = tile + kScaleBytes + 16 * lane;
+  const uint8_t* xb = xs + 8 * (lane & 7);
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    unsigned long long v0, v1;  // words (0, 1): elements 0..15; words (2, 3): 16..31
-    asm volatile("ld.shared.v2.b64 {%0, %1}, [%2];"
-                 : "=l"(v0), "=l"(v1)
-                 : "r"(tile + kScaleBytes + kCodeRowBytes * j + 16 * lane));
-    unsigned long long acc = pair_dot(v0, xb, c, 0ull, true);
-    acc = pair_dot(v1, xb + 8, c, acc, false);
-    const f2 a = unpack2(acc);
-    yv[j] = fmaf(a.x + a.y, d[j], yv[j]);
+    const uint4 w4 = *reinterpret_cast<const uint4*>(codes + kStepBytes * j);
+    const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {  // block 2j + h = steps 4j + 2h, 4j + 2h + 1
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int s = 4 * j + 2 * h + u;
+        uint2 b = make_uint2(0u, 0u);
+        if (bl) b = *reinterpret_cast<const uint2*>(xb + s * kXStepBytes);
+        uint32_t a[4];
+        decode_step(w[2 * h + u], a);
+        mma_f16(d, a, b.x, b.y);
+      }
+      const int blk = 2 * j + h;
+      const float d0 = half_bits_to_float(sw[blk]) * f[blk];
+      const float d1 = half_bits_to_float(sw[blk] >> 16) * f[blk];
+      y[0] = fmaf(d[0] + d[1], d0, y[0]);
+      y[1] = fmaf(d[2] + d[3], d1, y[1]);
+    }
   }
 }
 

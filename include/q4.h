@@ -211,14 +211,18 @@ q4_status q4_embed_gather(const void* table, int64_t vocab, int64_t k, const int
  * q4_repack copies a GGUF Q4_0 matrix into this library's GPU layout (the pages
  * name only the GGUF format, "Arquitectura"; the layout below is a packaging
  * choice, every block's bytes are kept): rows in groups of 16, k in slices of
- * 256 (8 blocks); tile (g, t) = rows 16g..16g+15 x blocks 8t..8t+7 is 2304
- * bytes at (g * k/256 + t) * 2304; inside it, for lane L = 8h + b (h = 0..3,
- * b = 0..7) and j = 0..3, the binary16 scale of row 16g + 4h + j, block
- * 8t + b sits at byte 8L + 2j and its codes at 256 + 512j + 16L as four
- * little-endian words, nibble m of word u holding element 16 (u / 2) + 2m +
- * (u % 2) of the block.
+ * 256 (8 blocks); tile (G, t) = rows 16G..16G+15 x blocks 8t..8t+7 is 2304
+ * bytes at (G * k/256 + t) * 2304.  Inside it, for g = 0..7 and hr = 0 (row
+ * 16G + g) or 1 (row 16G + g + 8):
+ *   scales: the binary16 d of block 8t + b of that row at byte 32g + 4b + 2hr;
+ *   codes: column c = 16s + i of the tile (step s = 0..15) belongs to lane
+ *   L = 4g + (i % 8) / 2 of step s, whose little-endian 32-bit word at
+ *   256 + 512 (s / 4) + 16L + 4 (s % 4) holds the code in its nibble
+ *   m = hr + 2 (i / 8) + 4 (i % 2) (bits 4m..4m+3).
+ * That is the operand order of a 16 x 16 row-major tensor-core A fragment:
+ * one word per lane and step, four steps per 16-byte load.
  * Rows past n in the last group are d = +0 with every code 8.  Each tile is
- * one contiguous 16-byte-aligned run that a warp reads in whole 16-byte words.
+ * one contiguous 16-byte-aligned run.
  *   W  GGUF Q4_0 [n rows of k/32 blocks], 16-byte aligned; k % 256 == 0.
  *   R  output, q4_repack_bytes(n, k) bytes, 16-byte aligned, must not overlap W.
  * q4_repack_bytes returns 0 for a shape it does not take. */
@@ -266,7 +270,13 @@ typedef struct q4_chain_link {
  *   p_s[r] = sum_j w^_s[r][j] x_s[j],  x_s = src(x)
  *   y_s = p_s (+ src(residual)), or the gated pairs of p_s with Q4_OP_SWIGLU
  * Each p_s is within 1e-4 * (sum_j |w^ x_s| + |residual|) of the exact value
- * for the x_s it read; sums over split work are added in a fixed order, so
+ * for the x_s it read, x_s finite.  The products run on the tensor cores:
+ * each 32-element block of x_s is scaled by a power of two that puts its
+ * largest magnitude in [2^14, 2^15) and carried as a binary16 pair hi + lo
+ * (relative error below 2^-22), so an element more than ~2^38 below its
+ * block's largest magnitude, or in a block whose largest magnitude is below
+ * 2^-112, may count as zero; a non-finite element of x_s makes outputs
+ * non-finite.  Sums over split work are added in a fixed order, so
  * results do not depend on timing, and a y_s written to memory is bitwise the
  * value later links read.  Q4_OP_ARGMAX writes the index of the largest y
  * (lowest index among equal values; NaN never wins; -1 if every y is NaN) and
@@ -281,8 +291,9 @@ typedef struct q4_chain_link {
  *              is fine on a used workspace (its first call is a little slower).
  * The launch is cooperative (one CTA per SM, all resident): Q4_ERR_CUDA if the
  * GPU cannot hold them.  A shape whose per-SM bookkeeping would not fit the
- * kernel's shared memory returns Q4_ERR_UNSUPPORTED_SHAPE (n up to ~2.6
- * million rows at k = 3072 fit; with a residual, ~470 thousand). */
+ * kernel's shared memory returns Q4_ERR_UNSUPPORTED_SHAPE (at k = 3072, n up
+ * to about 260 thousand rows fits, the 131072-row output head included; with
+ * a residual, about 150 thousand). */
 size_t q4_chain_workspace_bytes(const q4_chain_link* links, int32_t n_links);
 q4_status q4_chain(const q4_chain_link* links, int32_t n_links, void* workspace, size_t ws_bytes,
                    int32_t* status_dev, uint32_t flags, q4_stream_t s);
