@@ -35,10 +35,11 @@
 //     sets of slots used by alternate launches; each launch puts the set the
 //     next launch will use back to that pattern, and the last CTA to finish
 //     puts the counters back to zero.
-//   * The staged input is split for the tensor cores: each 32-element block is
-//     scaled by a power of two that puts its largest magnitude in
+//   * The staged input is split for the tensor cores: each 256-element slice
+//     is scaled by a power of two that puts its largest magnitude in
 //     [2^14, 2^15) and carried as a binary16 pair hi + lo (relative error
-//     below 2^-22); the block's inverse scale is applied to the fp32 sums.
+//     below 2^-22); the slice's inverse scale is applied to each tile's fp32
+//     sums.
 //   * An output with the argmax op is reduced without writing it: each CTA
 //     takes the largest of the rows it finishes, and CTA 0 reduces the CTAs'
 //     records at the end of the launch.
@@ -63,16 +64,19 @@ constexpr int kWarpGroups = 8;       // 16-row groups one warp may touch in one 
 constexpr int kCtaGroups = 64;       // groups one CTA may first-own in a link with a residual
 constexpr int kMaxLinks = Q4_CHAIN_MAX_LINKS;
 constexpr int kMaxK = 12288;
-constexpr int kStageQuads = 2;       // element quads per thread and staging pass
+constexpr int kStageQuads = 2;       // element quads per thread and staging pass: a warp
+                                     // stages one 256-element slice
 constexpr int kSlotFloats = 16;      // one 16-row group partial
 constexpr uint32_t kEmpty = 0x7FBADBADu;  // NaN pattern that no arithmetic produces
-constexpr int kHeaderBytes = 1024;
+constexpr int kHeaderBytes = 4096;
 // header words (uint32): epoch, finished-CTA counter, abort flag, reset barrier,
-// clean extent of buffer 0 / 1 (floats), each on its own 64-byte line; then
-// one done-CTA counter per link
+// clean extent of buffer 0 / 1 (floats), the one-product kernel's ticket, each
+// on its own 64-byte line; one done-CTA counter per link; from byte 1024 the
+// one-product kernel's argmax records (2 words per CTA)
 constexpr int kHdrEpoch = 0, kHdrFinished = 16, kHdrAbort = 32, kHdrBarrier = 48;
-constexpr int kHdrClean0 = 64, kHdrClean1 = 80, kHdrCount = 128;
-static_assert(kHdrCount + kMaxLinks <= kHeaderBytes / 4, "header");
+constexpr int kHdrClean0 = 64, kHdrClean1 = 80, kHdrTicket = 96, kHdrCount = 128;
+constexpr int kHdrRecords = 256, kMaxCtas = (kHeaderBytes / 4 - kHdrRecords) / 2;
+static_assert(kHdrCount + kMaxLinks <= kHdrRecords, "header");
 
 // floor(n / d) for 32-bit n by a multiply-high and a shift (constants made on
 // the host), then checked exactly.
@@ -209,7 +213,7 @@ struct Ctx {
 __device__ __noinline__ void fail(Ctx& x) {
   if (atomicExch(x.s_abort, 1) == 0) {
     report(x.status, 6 /* Q4_ERR_TIMEOUT */);
-    atomicExch(x.hdr + kHdrAbort, 1u);
+    if (x.hdr != nullptr) atomicExch(x.hdr + kHdrAbort, 1u);
   }
 }
 
@@ -218,7 +222,8 @@ __device__ __forceinline__ bool keep_waiting(Ctx& x, int& spins) {
   if (spins >= 8) __nanosleep(64);
   if ((++spins & 15) != 0) return true;
   if (*reinterpret_cast<volatile int*>(x.s_abort)) return false;
-  if (ld_relaxed_u32(x.hdr + kHdrAbort) != 0u || global_timer_ns() - x.t0 > kWaitLimitNs) {
+  if ((x.hdr != nullptr && ld_relaxed_u32(x.hdr + kHdrAbort) != 0u) ||
+      global_timer_ns() - x.t0 > kWaitLimitNs) {
     fail(x);
     return false;
   }
@@ -324,14 +329,20 @@ __device__ __forceinline__ bool load_entries(const Ent (&en)[W], Ctx& x, float4 
   return true;
 }
 
-// The x entries of staging pass `pass`: element quads tid + (pass W + m) kThreads.
+// The element quad that lane `lane` of warp `warp` stages as its m-th in pass
+// `pass`: warp w stages slice 16 pass + w, two quads per lane.
+__device__ __forceinline__ int stage_quad(int pass, int warp, int lane, int m) {
+  return 64 * (pass * kWarps + warp) + 32 * m + lane;
+}
+
+// The x entries of staging pass `pass`.
 __device__ __forceinline__ void x_entries(const SLink* sl, float* set_base, const SLink& S,
                                           int pass, int tid, uint32_t C,
                                           Ent (&en)[kStageQuads + 1]) {
   const int quads = S.k / 4;
 #pragma unroll
   for (int m = 0; m < kStageQuads; ++m) {
-    const int q = tid + (pass * kStageQuads + m) * kThreads;
+    const int q = stage_quad(pass, tid >> 5, tid & 31, m);
     en[m].np = -1;
     if (q < quads) en[m] = make_entry(sl, set_base, S.ext[0], S.src_link[0], S.src_off[0] + 4 * q, C);
   }
@@ -339,26 +350,28 @@ __device__ __forceinline__ void x_entries(const SLink* sl, float* set_base, cons
 
 __device__ __forceinline__ float silu_gate(float a, float b) { return a / (1.0f + __expf(-a)) * b; }
 
-// Staged x for the tensor cores: every 32-element block scaled by a power of
-// two and split into binary16 hi + lo (q4r_tile.cuh layout), its inverse
-// scale in xinv.  The eight lanes 8j..8j+7 of a warp hold the eight quads of
-// one block (kThreads and the pass stride are multiples of 8).
+// Staged x for the tensor cores: every 256-element slice (one warp's two
+// quads per lane) scaled by a power of two and split into binary16 hi + lo
+// (q4r_tile.cuh layout), its inverse scale in xinv[slice].  A warp's quads
+// are all valid or all past k (k % 256 == 0).
 __device__ __forceinline__ void convert_x(const float4 (&v)[kStageQuads + 1],
                                           const Ent (&en)[kStageQuads + 1], int pass, int tid,
                                           uint8_t* x16, float* xinv) {
+  const int warp = tid >> 5, lane = tid & 31;
+  float amax = 0.f;
+#pragma unroll
+  for (int m = 0; m < kStageQuads; ++m)
+    if (en[m].np >= 0)
+      amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[m].x), fabsf(v[m].y)),
+                               fmaxf(fabsf(v[m].z), fabsf(v[m].w))));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  float sc, inv;
+  rt::slice_scale(amax, sc, inv);
 #pragma unroll
   for (int m = 0; m < kStageQuads; ++m) {
-    const bool valid = en[m].np >= 0;
-    const int e = 4 * (tid + (pass * kStageQuads + m) * kThreads);
-    float amax = valid ? fmaxf(fmaxf(fabsf(v[m].x), fabsf(v[m].y)),
-                               fmaxf(fabsf(v[m].z), fabsf(v[m].w)))
-                       : 0.f;
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
-    if (!valid) continue;
-    float sc, inv;
-    rt::block_scale(amax, sc, inv);
+    if (en[m].np < 0) continue;
+    const int e = 4 * stage_quad(pass, warp, lane, m);
     __half h[4], l[4];
     rt::split_hi_lo(v[m].x * sc, h[0], l[0]);
     rt::split_hi_lo(v[m].y * sc, h[1], l[1]);
@@ -369,7 +382,7 @@ __device__ __forceinline__ void convert_x(const float4 (&v)[kStageQuads + 1],
     *reinterpret_cast<__half2*>(x16 + rt::x16_word(s, 0, i0 + 2)) = __halves2half2(h[2], h[3]);
     *reinterpret_cast<__half2*>(x16 + rt::x16_word(s, 1, i0)) = __halves2half2(l[0], l[1]);
     *reinterpret_cast<__half2*>(x16 + rt::x16_word(s, 1, i0 + 2)) = __halves2half2(l[2], l[3]);
-    if ((tid & 7) == 0) xinv[e >> 5] = inv;
+    if (m == 0 && lane == 0) xinv[e >> 8] = inv;
   }
 }
 
@@ -469,8 +482,8 @@ __device__ __noinline__ bool run_tiles(const SLink* sl, int n_links, TileStream&
           if (cur >= 0) flush(cur);
           cur = g;
         }
-        rt::tile_dot(chunk + p * rt::kTileBytes, x16 + t * (16 * rt::kXStepBytes), xinv + 8 * t,
-                     lane, y);
+        rt::tile_dot(chunk + p * rt::kTileBytes, x16 + t * (16 * rt::kXStepBytes), xinv[t], lane,
+                     y);
         if (++t == nsb) {
           t = 0;
           ++g;
@@ -509,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
   x.hdr = A.hdr;
   x.status = A.status;
   const int n_links = A.n_links;
-  // dynamic shared memory: ring | staged x | inverse block scales
+  // dynamic shared memory: ring | staged x | inverse slice scales
   uint8_t* const ring_p = smem + warp * kSlots * kChunkBytes;
   const uint32_t ring = smem_u32(ring_p);
   uint8_t* const x16 = smem + kWarps * kSlots * kChunkBytes;
@@ -712,7 +725,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
         if (en[kStageQuads].np >= 0)
           *reinterpret_cast<float4*>(&sres[tid / 4][4 * (tid & 3)]) = v[kStageQuads];
       }
-      for (int pass = 1; ok && pass * kStageQuads * kThreads < S.k / 4; ++pass) {
+      for (int pass = 1; ok && pass * kWarps * 256 < S.k; ++pass) {
         x_entries(s_links, set_base, S, pass, tid, x.C, en);
         en[kStageQuads].np = -1;
         ok = load_entries(en, x, v);
@@ -846,6 +859,186 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
     }
   }
   // copies this warp still has in flight land before the CTA exits
+  for (int q = ts.consumed; q < ts.issued; ++q)
+    mbar_wait(bar0 + 8 * static_cast<uint32_t>(q % kSlots),
+              static_cast<uint32_t>((q / kSlots) & 1));
+}
+
+
+// ------------------------------------------------------------------ one product
+// A chain of one link needs no hand-off: CTA c takes whole 16-row groups
+// [G c / C, G (c+1) / C) (for the 131072-row output head the busiest CTA
+// holds 1.2 % more than the average), so every output is finished inside one
+// CTA, and the launch is an ordinary one.  Only the argmax crosses CTAs: each
+// CTA writes a record, takes a ticket, and the CTA with the last ticket reduces
+// the records (nothing waits).
+struct SingleArgs {
+  const uint8_t* R;
+  const float* x;         // k elements (offset applied)
+  const float* residual;  // n elements, or nullptr
+  float* y;               // or nullptr
+  int32_t* argmax;        // or nullptr
+  uint32_t* hdr;          // workspace header (ticket, records)
+  int32_t* status;
+  int32_t n, k, nsb, groups;
+  uint32_t ops, flags;
+};
+
+__global__ void __launch_bounds__(kThreads, 1) single_kernel(const SingleArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t full_bar[kWarps][kSlots];
+  __shared__ __align__(8) uint64_t never_bar;
+  __shared__ __align__(16) float P[kWarps][kWarpGroups][kSlotFloats];
+  __shared__ __align__(16) SLink s_link[1];
+  __shared__ int s_wa[kWarps], s_wb[kWarps];
+  __shared__ int2 s_wg[kWarps];
+  __shared__ float s_bv[kWarps];
+  __shared__ int s_bi[kWarps];
+  __shared__ int s_abort, s_last;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t c = blockIdx.x, C = gridDim.x;
+  Ctx x;
+  x.c = c;
+  x.C = C;
+  x.s_abort = &s_abort;
+  x.hdr = nullptr;  // no cross-CTA abort flag: nothing here waits on another CTA
+  x.status = a.status;
+  uint8_t* const ring_p = smem + warp * kSlots * kChunkBytes;
+  const uint32_t ring = smem_u32(ring_p);
+  uint8_t* const x16 = smem + kWarps * kSlots * kChunkBytes;
+  float* const xinv = reinterpret_cast<float*>(x16 + rt::x16_bytes(a.k));
+  const uint32_t bar0 = smem_u32(&full_bar[warp][0]);
+  const uint64_t pol = l2_evict_first_policy();
+  const int g0c = static_cast<int>(static_cast<int64_t>(a.groups) * c / C);
+  const int g1c = static_cast<int>(static_cast<int64_t>(a.groups) * (c + 1) / C);
+  const int ca = g0c * a.nsb, cb = g1c * a.nsb, gcount = g1c - g0c;
+  if (tid == 0) {
+    s_abort = 0;
+    mbar_init(smem_u32(&never_bar), 1);
+    SLink& S = s_link[0];
+    S.R = a.R;
+    S.ext[0] = a.x;
+    S.src_link[0] = -1;
+    S.src_off[0] = 0;
+    S.ca = ca;
+    S.cb = cb;
+    S.nsb = a.nsb;
+    S.k = a.k;
+  }
+  if (lane == 0) {
+    for (int i = 0; i < kSlots; ++i) mbar_init(bar0 + 8 * i, 1);
+    int wa, wb;
+    warp_range(ca, cb, warp, wa, wb);
+    s_wa[warp] = wa;
+    s_wb[warp] = wb;
+    s_wg[warp] = wa < wb ? make_int2(wa / a.nsb, (wb - 1) / a.nsb) : make_int2(1, 0);
+  }
+  fence_mbarrier_init();
+  __syncthreads();
+  TileStream ts;
+  ts.ps = 0;
+  ts.issued = 0;
+  ts.consumed = 0;
+  stream_enter(s_link, ts, warp);
+  stream_settle(s_link, 1, ts, warp);
+  for (int i = 0; i < kSlots; ++i) stream_issue(s_link, 1, ts, warp, lane, ring, bar0, pol);
+  volatile int* abort_flag = &s_abort;
+  if ((a.flags & kFlagTestStallOneWait) != 0 && c == 0 && tid == 0)
+    if (!mbar_wait(smem_u32(&never_bar), 0, &s_abort)) fail(x);
+
+  // ---- stage x
+  if (gcount > 0) {
+    const SLink& S = s_link[0];
+    Ent en[kStageQuads + 1];
+    float4 v[kStageQuads + 1];
+    en[kStageQuads].np = -1;
+    for (int pass = 0; pass * kWarps * 256 < a.k; ++pass) {
+      x_entries(s_link, nullptr, S, pass, tid, C, en);
+      load_entries(en, x, v);  // plain loads: nothing to wait for
+      convert_x(v, en, pass, tid, x16, xinv);
+    }
+  }
+  bool stop = __syncthreads_or(*abort_flag) != 0;
+
+  // ---- tiles, then the CTA's groups
+  float bv = 0.f;
+  int bi = -1;
+  if (!stop) {
+    run_tiles(s_link, 1, ts, x, warp, lane, ring_p, ring, bar0, x16, xinv, s_wa[warp], s_wb[warp],
+              s_wg[warp].x, a.nsb, P[warp]);
+    stop = __syncthreads_or(*abort_flag) != 0;
+  }
+  if (!stop && (a.ops & kOpSwiglu)) {
+    for (int idx = tid; idx < gcount * 8; idx += kThreads) {
+      const int gl = idx >> 3, j = idx & 7, g = g0c + gl;
+      float va = 0.f, vb = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const int2 r = s_wg[w];
+        if (g >= r.x && g <= r.y) {
+          va += P[w][g - r.x][j];
+          vb += P[w][g - r.x][j + 8];
+        }
+      }
+      const float v = silu_gate(va, vb);
+      if (a.y != nullptr) a.y[8 * g + j] = v;
+      better(bv, bi, v, 8 * g + j);
+    }
+  } else if (!stop) {
+    for (int idx = tid; idx < gcount * kSlotFloats; idx += kThreads) {
+      const int gl = idx >> 4, row16 = idx & 15, g = g0c + gl, row = 16 * g + row16;
+      float sum = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const int2 r = s_wg[w];
+        if (g >= r.x && g <= r.y) sum += P[w][g - r.x][row16];
+      }
+      if (row < a.n) {
+        if (a.residual != nullptr) sum += __ldcg(a.residual + row);
+        if (a.y != nullptr) a.y[row] = sum;
+        better(bv, bi, sum, row);
+      }
+    }
+  }
+  if (a.ops & kOpArgmax) {
+    // taken even after an abort, so that the tickets of every launch add up
+    warp_best(bv, bi);
+    if (lane == 0) {
+      s_bv[warp] = bv;
+      s_bi[warp] = bi;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      float v = 0.f;
+      int i = -1;
+      for (int w = 0; w < kWarps; ++w)
+        if (s_bi[w] >= 0) better(v, i, s_bv[w], s_bi[w]);
+      uint32_t* rec = a.hdr + kHdrRecords + 2 * c;
+      st_relaxed_u32(rec, __float_as_uint(i >= 0 ? v : 0.f));
+      st_relaxed_u32(rec + 1, static_cast<uint32_t>(i));
+      __threadfence();
+      s_last = atomicAdd(a.hdr + kHdrTicket, 1u) == C - 1;
+    }
+    __syncthreads();
+    if (s_last && warp == 0) {
+      // every record was written before its CTA's ticket: read them after ours
+      __threadfence();
+      float v = 0.f;
+      int i = -1;
+      for (uint32_t cc = lane; cc < C; cc += 32) {
+        const uint32_t* rec = a.hdr + kHdrRecords + 2 * cc;
+        const int ri = static_cast<int>(ld_relaxed_u32(rec + 1));
+        if (ri >= 0) better(v, i, __uint_as_float(ld_relaxed_u32(rec)), ri);
+      }
+      warp_best(v, i);
+      if (lane == 0) {
+        a.argmax[0] = i;
+        a.argmax[1] = __float_as_int(i >= 0 ? v : __uint_as_float(0x7FC00000u));
+        st_relaxed_u32(a.hdr + kHdrTicket, 0u);
+      }
+    }
+  }
   for (int q = ts.consumed; q < ts.issued; ++q)
     mbar_wait(bar0 + 8 * static_cast<uint32_t>(q % kSlots),
               static_cast<uint32_t>((q / kSlots) & 1));
@@ -1019,7 +1212,7 @@ q4_status chain_plan(const q4_chain_link* links, int32_t n, ChainArgs* A, size_t
 
 size_t chain_smem_bytes(int kmax) {
   return static_cast<size_t>(kWarps) * kSlots * kChunkBytes +
-         static_cast<size_t>(rt::x16_bytes(kmax)) + static_cast<size_t>(kmax / 32) * 4;
+         static_cast<size_t>(rt::x16_bytes(kmax)) + static_cast<size_t>(kmax / 256) * 4;
 }
 
 cudaError_t chain_launch(ChainArgs& A, void* workspace, cudaStream_t s) {
@@ -1048,6 +1241,45 @@ cudaError_t chain_launch(ChainArgs& A, void* workspace, cudaStream_t s) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, chain_kernel, A);
+}
+
+// One link (its sources are in memory): the one-product kernel, unless the
+// CTAs' whole-group shares do not fit its per-warp bookkeeping.
+bool single_fits(const q4_chain_link& l) {
+  const int64_t C = sm_count(), nsb = l.k / 256, groups = (l.n + 15) / 16;
+  if (C > kMaxCtas) return false;
+  const int64_t per_cta = (groups + C - 1) / C * nsb;
+  const int64_t per_warp = (per_cta + kWarps - 1) / kWarps;
+  return per_warp / nsb + 2 <= kWarpGroups;
+}
+
+cudaError_t single_launch(const q4_chain_link& l, void* workspace, int32_t* status, uint32_t flags,
+                          cudaStream_t s) {
+  SingleArgs a;
+  a.R = static_cast<const uint8_t*>(l.R);
+  a.x = l.x.ptr + l.x.offset;
+  a.residual = (l.ops & Q4_OP_RESIDUAL) ? l.residual.ptr + l.residual.offset : nullptr;
+  a.y = l.y;
+  a.argmax = l.argmax;
+  a.hdr = static_cast<uint32_t*>(workspace);
+  a.status = status;
+  a.n = static_cast<int32_t>(l.n);
+  a.k = static_cast<int32_t>(l.k);
+  a.nsb = static_cast<int32_t>(l.k / 256);
+  a.groups = static_cast<int32_t>((l.n + 15) / 16);
+  a.ops = l.ops;
+  a.flags = flags;
+  static bool configured[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(single_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(chain_smem_bytes(kMaxK)));
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  single_kernel<<<static_cast<unsigned>(sm_count()), kThreads, chain_smem_bytes(a.k), s>>>(a);
+  return cudaGetLastError();
 }
 
 cudaError_t repack_launch(const uint8_t* W, int64_t n, int64_t k, uint8_t* R, cudaStream_t s) {
@@ -1096,9 +1328,11 @@ q4_status q4_chain(const q4_chain_link* links, int32_t n_links, void* workspace,
   if (!q4::aligned(workspace, 256)) return Q4_ERR_MISALIGNED;
   A.status = status_dev;
   A.flags = flags;
-  return q4::chain_launch(A, workspace, reinterpret_cast<cudaStream_t>(s)) == cudaSuccess
-             ? Q4_OK
-             : Q4_ERR_CUDA;
+  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(s);
+  const cudaError_t e = (n_links == 1 && q4::single_fits(links[0]))
+                            ? q4::single_launch(links[0], workspace, status_dev, flags, cs)
+                            : q4::chain_launch(A, workspace, cs);
+  return e == cudaSuccess ? Q4_OK : Q4_ERR_CUDA;
 }
 
 static q4_chain_link one_link(const void* R, int64_t n, int64_t k, const float* x, float* y) {

@@ -30,11 +30,12 @@
 // mma.m16n8k16 (rows g and g + 8, columns 2t, 2t+1 and 2t+8, 2t+9).
 //
 // B: the activation x enters the tensor core as binary16, so it is carried as
-// an exact-to-2^-22 pair hi + lo in columns 0 and 1 of B (columns 2..7 are
-// zero), after scaling each 32-element block of x by a power of two that puts
+// an exact-to-2^-22 pair hi + lo in columns 0 and 1 of B (columns 2..7 repeat
+// them and are not read), after scaling each 256-element slice of x by a power of two that puts
 // its largest magnitude in [2^14, 2^15): rows g / g+8 of the result then sit in
 // the lanes t = 0 as D columns 0 (hi part) and 1 (lo part).  Per block the
-// fp32 fragment sums are multiplied by d and by the block's inverse scale.
+// fp32 fragment sums are multiplied by d, per tile by the slice's inverse
+// scale.
 #pragma once
 
 #include "q4_device.cuh"
@@ -61,9 +62,9 @@ __device__ __forceinline__ int x16_word(int s, int n, int i) {
   return s * kXStepBytes + (4 * n + ((i & 7) >> 1)) * 8 + ((i >> 3) << 2);
 }
 
-// Power-of-two scale for a block whose largest magnitude is amax: s puts amax
+// Power-of-two scale for a slice whose largest magnitude is amax: s puts amax
 // in [2^14, 2^15) (clamped to 2^-126 .. 2^126); returns s and 1/s, both exact.
-__device__ __forceinline__ void block_scale(float amax, float& s, float& inv) {
+__device__ __forceinline__ void slice_scale(float amax, float& s, float& inv) {
   const int ef = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFF);
   int se = 268 - ef;  // biased exponent of 2^(14 - (ef - 127))
   se = amax == 0.f ? 127 : (se < 1 ? 1 : (se > 253 ? 253 : se));
@@ -113,19 +114,17 @@ __device__ __forceinline__ void decode_step(uint32_t w, uint32_t (&a)[4]) {
 
 // One tile for this warp: y[0] += row g's and y[1] += row g+8's dot product
 // with the tile's 256 columns of x (meaningful in lanes with lane % 4 == 0;
-// the other lanes accumulate zeros).  tile: the landed tile; xs: the staged x
-// of the tile's slice (16 steps); xinv: the slice's 8 inverse block scales.
-__device__ __forceinline__ void tile_dot(const uint8_t* tile, const uint8_t* xs,
-                                         const float* xinv, int lane, float (&y)[2]) {
+// the other lanes accumulate copies of other columns).  tile: the landed tile; xs: the staged x
+// of the tile's slice (16 steps); xinv: the slice's inverse scale.
+__device__ __forceinline__ void tile_dot(const uint8_t* tile, const uint8_t* xs, float xinv,
+                                         int lane, float (&y)[2]) {
   const int g = lane >> 2;
-  const bool bl = lane < 8;  // lanes that carry B columns 0 and 1
   const uint4 sa = *reinterpret_cast<const uint4*>(tile + 32 * g);
   const uint4 sb = *reinterpret_cast<const uint4*>(tile + 32 * g + 16);
-  const float4 fa = *reinterpret_cast<const float4*>(xinv);
-  const float4 fb = *reinterpret_cast<const float4*>(xinv + 4);
   const uint32_t sw[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
-  const float f[8] = {fa.x, fa.y, fa.z, fa.w, fb.x, fb.y, fb.z, fb.w};
+  float yt[2] = {0.f, 0.f};
   const uint8_t* codes = tile + kScaleBytes + 16 * lane;
+  // lane 4n + t (n = 0, 1) carries B column n; lanes 8.. read the same words
   const uint8_t* xb = xs + 8 * (lane & 7);
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
@@ -137,19 +136,18 @@ __device__ __forceinline__ void tile_dot(const uint8_t* tile, const uint8_t* xs,
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const int s = 4 * j + 2 * h + u;
-        uint2 b = make_uint2(0u, 0u);
-        if (bl) b = *reinterpret_cast<const uint2*>(xb + s * kXStepBytes);
+        const uint2 b = *reinterpret_cast<const uint2*>(xb + s * kXStepBytes);
         uint32_t a[4];
         decode_step(w[2 * h + u], a);
         mma_f16(d, a, b.x, b.y);
       }
       const int blk = 2 * j + h;
-      const float d0 = half_bits_to_float(sw[blk]) * f[blk];
-      const float d1 = half_bits_to_float(sw[blk] >> 16) * f[blk];
-      y[0] = fmaf(d[0] + d[1], d0, y[0]);
-      y[1] = fmaf(d[2] + d[3], d1, y[1]);
+      yt[0] = fmaf(d[0] + d[1], half_bits_to_float(sw[blk]), yt[0]);
+      yt[1] = fmaf(d[2] + d[3], half_bits_to_float(sw[blk] >> 16), yt[1]);
     }
   }
+  y[0] = fmaf(yt[0], xinv, y[0]);
+  y[1] = fmaf(yt[1], xinv, y[1]);
 }
 
 }  // namespace rt

@@ -271,10 +271,10 @@ typedef struct q4_chain_link {
  *   y_s = p_s (+ src(residual)), or the gated pairs of p_s with Q4_OP_SWIGLU
  * Each p_s is within 1e-4 * (sum_j |w^ x_s| + |residual|) of the exact value
  * for the x_s it read, x_s finite.  The products run on the tensor cores:
- * each 32-element block of x_s is scaled by a power of two that puts its
+ * each 256-element slice of x_s is scaled by a power of two that puts its
  * largest magnitude in [2^14, 2^15) and carried as a binary16 pair hi + lo
  * (relative error below 2^-22), so an element more than ~2^38 below its
- * block's largest magnitude, or in a block whose largest magnitude is below
+ * slice's largest magnitude, or in a slice whose largest magnitude is below
  * 2^-112, may count as zero; a non-finite element of x_s makes outputs
  * non-finite.  Sums over split work are added in a fixed order, so
  * results do not depend on timing, and a y_s written to memory is bitwise the
