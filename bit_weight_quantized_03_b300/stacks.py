@@ -275,3 +275,64 @@ class EncoderStack:
                 for _ in range(passes):
                     self.forward(x_in, stream)
         return g
+
+
+class AdapterStack:
+    """The bridge from the 1280-wide encoder to the 3072-wide decoder
+    (GeekNews, "Arquitectura": "Conv with 4x downsampling -> adapter (3072
+    dimensions)"), as Q4_0 linears through q4_gemm.  Shapes are assumptions
+    (the pages give none): the downsampling conv has width and stride 4 over
+    time, i.e. it is a linear on 4 concatenated encoder frames (5120 -> 3072),
+    and the adapter is two linears 3072 -> 3072 -> 3072.  The 4-frame
+    concatenation is a reshape of the row-major [frames, 1280] encoder output
+    (no copy).  Activations between the linears are outside the Q4 path and
+    left out, as in the other stacks."""
+
+    def __init__(self, encoder_frames: int = synth.ADAPTER_ENCODER_FRAMES, config_id: int = 6,
+                 device="cuda"):
+        import torch
+        if encoder_frames % 4:
+            raise ValueError("encoder frames must be a multiple of 4")
+        self.torch = torch
+        self.device = torch.device(device)
+        self.frames = encoder_frames
+        self.m = encoder_frames // 4
+        self.mats = synth.ADAPTER_MATS
+        self.W = []
+        status = []
+        for idx, (_, n, k) in enumerate(self.mats):
+            blocks, st = _quantize_rows([(n, synth.seed_for(config_id, 0, idx))], k, self.device,
+                                        torch)
+            self.W.append(blocks)
+            status.append(st)
+        torch.cuda.synchronize()
+        if any(int(st.item()) != 0 for st in status):
+            raise RuntimeError("quantizing the adapter weights reported a device error")
+        bf = torch.bfloat16
+        self.Y = [torch.empty((self.m, n), dtype=bf, device=self.device) for _, n, _ in self.mats]
+        self.ws = Workspace(self.device)
+
+    def flops_per_pass(self) -> int:
+        return 2 * self.m * sum(n * k for _, n, k in self.mats)
+
+    def weight_bytes(self) -> int:
+        return sum(int(w.numel()) for w in self.W)
+
+    def forward(self, X_enc, stream=None, flags: int = FLAG_PDL):
+        """X_enc [frames, 1280] bf16 (row-major, contiguous) -> [frames/4, 3072] bf16."""
+        x = X_enc.reshape(self.m, 4 * X_enc.shape[1])
+        for W, (_, n, k), Y in zip(self.W, self.mats, self.Y):
+            q4_gemm(W, n, k, x, Y=Y, workspace=self.ws, flags=flags, stream=stream)
+            x = Y
+        return x
+
+    def capture(self, X_enc, stream, passes: int = 1):
+        torch = self.torch
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            self.forward(X_enc, stream)
+            stream.synchronize()
+            with torch.cuda.graph(g, stream=stream):
+                for _ in range(passes):
+                    self.forward(X_enc, stream)
+        return g

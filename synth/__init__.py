@@ -41,6 +41,15 @@ ENCODER_MATS = (("qkv", 3840, 1280), ("out", 1280, 1280), ("up", 5120, 1280),
                 ("down", 1280, 5120))
 ENCODER_FRAMES = (375, 1500, 3000)
 VOCAB = 131072
+# The bridge from the encoder to the decoder: "Conv with 4x downsampling ->
+# adapter (3072 dimensions)" (GeekNews es.news.hada.io/topic?id=26595,
+# "Arquitectura").  The pages give no kernel size or adapter depth; assumed
+# here: the 4x downsampling is a stride-4, width-4 convolution over time (a
+# linear on 4 concatenated 1280-wide encoder frames, 5120 -> 3072), then a
+# two-linear adapter 3072 -> 3072 -> 3072.  1500 encoder frames (30 s) give
+# 375 decoder-rate frames.
+ADAPTER_ENCODER_FRAMES = 1500
+ADAPTER_MATS = (("conv4x", 3072, 5120), ("adapter1", 3072, 3072), ("adapter2", 3072, 3072))
 
 
 def seed_for(config: int, layer: int = 0, matrix_index: int = 0) -> int:

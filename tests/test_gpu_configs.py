@@ -152,44 +152,109 @@ def test_config2_decode_step_exact_properties(torch, decoder):
     assert torch.equal(decoder.x, a * 2.0 ** -10)
 
 
-def test_config2_two_layer_chain_vs_oracle_chain(torch, q4, oracle_mod):
-    """Chain wiring: two decoder layers through DecoderStack.step against the
-    oracle applying the same eight products in the same order (fp32 between)."""
+def _oracle_mat(oracle_mod, torch, parts, l, rows=None):
+    """Oracle-quantized blocks of a row-concatenated decoder matrix (rows: a
+    subset of the concatenated rows, or all)."""
+    k = parts[0][1]
+    blocks, r0 = [], 0
+    for (n, _, idx) in parts:
+        sel = np.arange(n) if rows is None else rows[(rows >= r0) & (rows < r0 + n)] - r0
+        if sel.size:
+            blocks.append(_oracle_rows(oracle_mod, torch, n, k, synth.seed_for(2, l, idx), sel))
+        r0 += n
+    return np.concatenate(blocks), k
+
+
+PARTS = {"qkv": [(4096, 3072, 0), (1024, 3072, 1), (1024, 3072, 2)], "wo": [(3072, 4096, 3)],
+         "w13": [(9216, 3072, 4), (9216, 3072, 5)], "w2": [(3072, 9216, 6)]}
+
+
+def test_config2_two_layer_step_each_product_vs_oracle(torch, q4, oracle_mod):
+    """Two decoder layers through DecoderStack's per-launch step (PDL chain of
+    q4_gemv), one layer at a time: every product element-wise against the
+    oracle's fp64 product on the input that product read."""
     from bit_weight_quantized_03_b300.stacks import DecoderStack
     dec = DecoderStack(layers=2)
-    ref = []
-    for l in range(2):
-        mats = {}
-        for key, parts in {"qkv": [(4096, 3072, 0), (1024, 3072, 1), (1024, 3072, 2)],
-                           "wo": [(3072, 4096, 3)],
-                           "w13": [(9216, 3072, 4), (9216, 3072, 5)],
-                           "w2": [(3072, 9216, 6)]}.items():
-            blocks = []
-            for (n, k, idx) in parts:
-                w = synth.torch_weights(n, k, seed=synth.seed_for(2, l, idx)).cpu().numpy()
-                b, rc, _ = oracle_mod.quantize(w)
-                assert rc == 0
-                blocks.append(b)
-            mats[key] = (np.concatenate(blocks), sum(p[0] for p in parts), parts[0][1])
-        ref.append(mats)
-    x0 = synth.torch_activations(1, 3072, seed=synth.activation_seed(2000, 2))
-    dec.step(x0)
-    torch.cuda.synchronize()
-    got = dec.x.cpu().numpy().astype(np.float64)
     th = oracle_mod.cpu_count()
-    x = x0.cpu().numpy()
+    x = synth.torch_activations(1, 3072, seed=synth.activation_seed(2000, 2))
     for l in range(2):
-        W, n, k = ref[l]["qkv"]
-        y, _ = oracle_mod.matmul(W, n, k, x, nthreads=th)
-        W, n, k = ref[l]["wo"]
-        y, _ = oracle_mod.matmul(W, n, k, y[:, :4096].astype(np.float32), nthreads=th)
-        W, n, k = ref[l]["w13"]
-        y, _ = oracle_mod.matmul(W, n, k, y.astype(np.float32), nthreads=th)
-        W, n, k = ref[l]["w2"]
-        y, _ = oracle_mod.matmul(W, n, k, y[:, :9216].astype(np.float32), nthreads=th)
-        x = y.astype(np.float32)
-    rel = np.linalg.norm(got - y) / np.linalg.norm(y)
-    assert rel < 1e-4, rel
+        dec._layer(l, x, None)
+        torch.cuda.synchronize()
+        outs = {"qkv": dec.y_qkv.cpu().numpy(), "wo": dec.y_o.cpu().numpy(),
+                "w13": dec.y_13.cpu().numpy(), "w2": dec.x.cpu().numpy()}
+        ins = {"qkv": x.cpu().numpy(), "wo": outs["qkv"][:, :4096],
+               "w13": outs["wo"], "w2": outs["w13"][:, :9216]}
+        for key in ("qkv", "wo", "w13", "w2"):
+            W, k = _oracle_mat(oracle_mod, torch, PARTS[key], l)
+            n = W.shape[0]
+            Y, S = oracle_mod.matmul(W, n, k, np.ascontiguousarray(ins[key]), nthreads=th)
+            ok, info = within_tol(outs[key], Y, S, GEMV_TOL)
+            assert ok, (l, key, info)
+        x = dec.x.clone()
+
+
+def _gated_bound(a, b, Sa, Sb, tol):
+    """The product bounds tol*Sa, tol*Sb carried through g = a sigmoid(a) b,
+    plus the fp32 rounding of the gate itself."""
+    sig = 1.0 / (1.0 + np.exp(-a))
+    g = a * sig * b
+    return (tol * Sa * np.abs(b) * (sig + np.abs(a) * sig * (1 - sig)) +
+            tol * Sb * np.abs(a * sig) + 1e-6 * np.abs(g) + 1e-30), g
+
+
+def test_config2_fused_step_26_layers_sampled_vs_oracle(torch, q4, oracle_mod, decoder):
+    """The full 26-layer decode step as one q4_chain on the repacked weights,
+    with the gated FFN and both residual adds fused, every link writing its
+    output: sampled rows of each of the 104 links element-wise against the
+    oracle on the input that link read (weights from the oracle's own
+    quantization of the seeded matrices).  The synthetic decoder has no norms
+    (they are outside the Q4 path) and its gated FFN is quadratic in the scale
+    of its input, so an N(0, 1) input overflows fp32 within a few layers; the
+    input is scaled by 2^-24, which keeps all 26 layers finite (the slice
+    scaling of the staged x is exact under powers of two)."""
+    H, Q, F = 3072, 4096, 9216
+    outs = []
+    for l in range(decoder.layers):
+        for n in (Q + 2048, H, F, H):
+            outs.append(torch.full((n,), float("nan"), device="cuda"))
+    x0 = synth.torch_activations(1, H, seed=synth.activation_seed(2000, 9)) * 2.0 ** -24
+    decoder.fused_step(x0, outs=outs)
+    torch.cuda.synchronize()
+    got = [o.cpu().numpy().astype(np.float64) for o in outs]
+    x_l = x0.cpu().numpy()[0]
+    for l in range(decoder.layers):
+        b = 4 * l
+        y_qkv, h, g, x_next = got[b:b + 4]
+        sel = lambda n, i: _sample_rows(n, 16, seed=1000 * l + i)  # noqa: E731
+        # qkv = Wqkv x_l
+        r = sel(Q + 2048, 0)
+        W, k = _oracle_mat(oracle_mod, torch, PARTS["qkv"], l, r)
+        Y, S = oracle_mod.matmul(W, len(r), k, x_l.astype(np.float32))
+        ok, info = within_tol(y_qkv[r], Y[0], S[0], GEMV_TOL)
+        assert ok, (l, "qkv", info)
+        # h = x_l + Wo q
+        r = sel(H, 1)
+        W, k = _oracle_mat(oracle_mod, torch, PARTS["wo"], l, r)
+        Y, S = oracle_mod.matmul(W, len(r), k, y_qkv[:Q].astype(np.float32))
+        ok, info = within_tol(h[r], Y[0] + x_l[r], S[0] + np.abs(x_l[r]), GEMV_TOL)
+        assert ok, (l, "wo + residual", info)
+        # g = silu(W1 h) * (W3 h)
+        r = sel(F, 2)
+        W1, k = _oracle_mat(oracle_mod, torch, PARTS["w13"][:1], l, r)
+        W3, _ = _oracle_mat(oracle_mod, torch, [(F, H, 5)], l, r)
+        A, Sa = oracle_mod.matmul(W1, len(r), k, h.astype(np.float32))
+        B, Sb = oracle_mod.matmul(W3, len(r), k, h.astype(np.float32))
+        bound, gref = _gated_bound(A[0], B[0], Sa[0], Sb[0], GEMV_TOL)
+        err = np.abs(g[r] - gref)
+        assert np.all(err <= bound), (l, "gate", float(np.max(err / bound)))
+        # x_{l+1} = h + W2 g
+        r = sel(H, 3)
+        W, k = _oracle_mat(oracle_mod, torch, PARTS["w2"], l, r)
+        Y, S = oracle_mod.matmul(W, len(r), k, g.astype(np.float32))
+        ok, info = within_tol(x_next[r], Y[0] + h[r], S[0] + np.abs(h[r]), GEMV_TOL)
+        assert ok, (l, "w2 + residual", info)
+        assert np.all(np.isfinite(x_next)), l
+        x_l = x_next.astype(np.float32)
 
 
 # --------------------------------------------------------------------- config 3
