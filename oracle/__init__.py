@@ -84,6 +84,10 @@ def lib():
             L.q4o_swiglu.restype = None
             L.q4o_argmax.argtypes = [f64p, i64]
             L.q4o_argmax.restype = i64
+            L.q4o_quantize_q8.argtypes = [f32p, i64, ctypes.POINTER(ctypes.c_int8), f32p]
+            L.q4o_quantize_q8.restype = ctypes.c_int
+            L.q4o_matmul_q8.argtypes = [u8p, i64, i64, f32p, i64, i64, f64p, f64p, i64]
+            L.q4o_matmul_q8.restype = ctypes.c_int
             L.q4o_repack_bytes.argtypes = [i64, i64]
             L.q4o_repack_bytes.restype = i64
             L.q4o_repack.argtypes = [u8p, i64, i64, u8p]
@@ -164,6 +168,34 @@ def matmul(W: np.ndarray, n: int, k: int, X: np.ndarray, nthreads: int = 1):
                           _ptr(Y, ctypes.c_double), _ptr(S, ctypes.c_double), n, int(nthreads))
     if rc != OK:
         raise ValueError("q4o_matmul: invalid arguments")
+    return Y, S
+
+
+def quantize_q8(x: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
+    """fp32 x [k] -> (int8 codes [k], fp32 block scales [k/32]) (Q4 x Q8 reading)."""
+    x = np.ascontiguousarray(x, dtype=np.float32).ravel()
+    q = np.empty(x.size, np.int8)
+    d = np.empty(x.size // BLOCK_ELEMS, np.float32)
+    rc = lib().q4o_quantize_q8(_ptr(x, ctypes.c_float), x.size, _ptr(q, ctypes.c_int8),
+                               _ptr(d, ctypes.c_float))
+    if rc != OK:
+        raise ValueError("q4o_quantize_q8: invalid arguments")
+    return q, d
+
+
+def matmul_q8(W: np.ndarray, n: int, k: int, X: np.ndarray):
+    """Q4 x Q8 product: fp64 Y[m, n] and S[m, n] (each row of X quantized per 32)."""
+    W = _blocks(W, n, k)
+    X = np.ascontiguousarray(np.atleast_2d(X), dtype=np.float32)
+    m = X.shape[0]
+    if X.shape[1] != k:
+        raise ValueError("X has the wrong width")
+    Y = np.empty((m, n), np.float64)
+    S = np.empty((m, n), np.float64)
+    rc = lib().q4o_matmul_q8(_ptr(W, ctypes.c_uint8), n, k, _ptr(X, ctypes.c_float), m, k,
+                             _ptr(Y, ctypes.c_double), _ptr(S, ctypes.c_double), n)
+    if rc != OK:
+        raise ValueError("q4o_matmul_q8: invalid arguments")
     return Y, S
 
 

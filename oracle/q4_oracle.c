@@ -356,6 +356,89 @@ int q4o_unrepack(const uint8_t* R, int64_t n, int64_t k, uint8_t* W) {
   return Q4O_OK;
 }
 
+/* ---------------------------------------------------------------- Q4 x Q8 */
+
+/* READING: the pages name only GGUF Q4_0 ("Arquitectura"); the integer path is
+ * the usual companion of that format, and its details are this library's
+ * choice.  x is quantized per 32-element block to int8 with an fp32 scale:
+ * amax = max |x_j|, d = amax / 127 (fp32 IEEE division), q_j = x_j / d (fp32
+ * IEEE division) rounded to the nearest integer with halves away from zero,
+ * clamped to [-127, 127].  amax == 0 gives d = +0 and every q_j = 0; a block
+ * holding a NaN or an infinity gives d = NaN and every q_j = 0. */
+int q4o_quantize_q8(const float* x, int64_t k, int8_t* q, float* d) {
+  if (!x || !q || !d || k <= 0 || k % 32) return Q4O_ERR_INVALID_ARG;
+  for (int64_t b = 0; b < k / 32; ++b) {
+    const float* xb = x + 32 * b;
+    float amax = 0.0f;
+    int finite = 1;
+    for (int j = 0; j < 32; ++j) {
+      if (!isfinite(xb[j])) finite = 0;
+      float a = fabsf(xb[j]);
+      if (a > amax) amax = a;
+    }
+    if (!finite) {
+      d[b] = NAN;
+      for (int j = 0; j < 32; ++j) q[32 * b + j] = 0;
+      continue;
+    }
+    float db = amax / 127.0f;
+    d[b] = db;
+    for (int j = 0; j < 32; ++j) {
+      float c = 0.0f;
+      if (db != 0.0f) {
+        float t = xb[j] / db;
+        c = roundf(t); /* halves away from zero */
+        if (c > 127.0f) c = 127.0f;
+        if (c < -127.0f) c = -127.0f;
+      }
+      q[32 * b + j] = (int8_t)c;
+    }
+  }
+  return Q4O_OK;
+}
+
+/* The Q4 x Q8 product of every row of X (each quantized as above) with W:
+ *   y_r = sum_b d_w[r,b] * d_x[b] * sum_{j in b} (q_w[r,j] - 8) * q_x[j]
+ * with the integer sums exact and the rest in fp64; S_r = sum_b of the
+ * magnitudes of those block terms. */
+int q4o_matmul_q8(const uint8_t* W, int64_t n, int64_t k, const float* X, int64_t m,
+                  int64_t ldx, double* Y, double* S, int64_t ldy) {
+  if (!W || !X || !Y || n < 0 || m < 0 || k <= 0 || k % 32 || ldx < k || ldy < n)
+    return Q4O_ERR_INVALID_ARG;
+  int64_t nb = k / 32;
+  int8_t* q = (int8_t*)malloc((size_t)k);
+  float* dx = (float*)malloc((size_t)nb * sizeof(float));
+  if (!q || !dx) {
+    free(q);
+    free(dx);
+    return Q4O_ERR_INVALID_ARG;
+  }
+  for (int64_t mm = 0; mm < m; ++mm) {
+    q4o_quantize_q8(X + mm * ldx, k, q, dx);
+    for (int64_t i = 0; i < n; ++i) {
+      double y = 0.0, s = 0.0;
+      for (int64_t b = 0; b < nb; ++b) {
+        const uint8_t* blk = W + (i * nb + b) * 18;
+        double dw = (double)q4o_half_to_float((uint16_t)(blk[0] | (blk[1] << 8)));
+        int64_t isum = 0;
+        for (int j = 0; j < 16; ++j) {
+          int lo = blk[2 + j] & 0x0F, hi = blk[2 + j] >> 4;
+          isum += (int64_t)(lo - 8) * q[32 * b + j];
+          isum += (int64_t)(hi - 8) * q[32 * b + j + 16];
+        }
+        double t = dw * (double)dx[b] * (double)isum;
+        y += t;
+        s += fabs(t);
+      }
+      Y[mm * ldy + i] = y;
+      if (S) S[mm * ldy + i] = s;
+    }
+  }
+  free(q);
+  free(dx);
+  return Q4O_OK;
+}
+
 /* ---------------------------------------------------------------- gather */
 
 /* READING: the pages look rows up on the CPU; the lookup itself is "row id ->

@@ -89,6 +89,18 @@ void q4o_swiglu(const double* a, const double* b, int64_t n, double* out);
  * Returns -1 when n <= 0 or every entry is NaN. */
 int64_t q4o_argmax(const double* y, int64_t n);
 
+/* Q4 x Q8 integer path (READING: the usual companion of GGUF Q4_0; details
+ * are this library's).  q4o_quantize_q8: x [k] (k % 32 == 0) -> int8 codes q
+ * [k] and fp32 scales d [k/32]: amax = max |x_j| per block, d = amax / 127,
+ * q_j = round-half-away(x_j / d) clamped to +-127 (fp32 IEEE division);
+ * amax == 0 -> d = +0, q = 0; a non-finite element -> d = NaN, q = 0.
+ * q4o_matmul_q8: Y[m][n] = sum_b d_w * d_x * sum_j (q_w - 8) q_x per row of X
+ * (integer sums exact, the rest fp64), S the sum of the block terms'
+ * magnitudes.  Return Q4O_OK or Q4O_ERR_INVALID_ARG. */
+int q4o_quantize_q8(const float* x, int64_t k, int8_t* q, float* d);
+int q4o_matmul_q8(const uint8_t* W, int64_t n, int64_t k, const float* X, int64_t m,
+                  int64_t ldx, double* Y, double* S, int64_t ldy);
+
 /* Repacked tile layout of a Q4_0 matrix (this library's GPU-native layout;
  * the pages name only the GGUF format).  Definition, for k % 256 == 0:
  *   rows are taken in groups of 16 (the last group padded with rows whose

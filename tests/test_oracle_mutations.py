@@ -1,6 +1,6 @@
 """Plants plausible mistakes in a temporary copy of the CPU oracle and checks that
-the oracle's pins (tests/test_oracle_pins.py, tests/test_oracle_pins_glue.py)
-fail for each one.  The repository's
+the oracle's pins (tests/test_oracle_pins.py, tests/test_oracle_pins_glue.py,
+tests/test_oracle_pins_q8.py) fail for each one.  The repository's
 oracle is never modified; each mutant is compiled and tested in a temp folder."""
 import os
 import shutil
@@ -45,6 +45,15 @@ MUTANTS = {
     "repack_scale_slot": ("*scale_off = tile + 32 * g + 4 * b + 2 * hr;",
                           "*scale_off = tile + 32 * b + 4 * g + 2 * hr;"),
     "repack_pad_code": ("int q = 8;", "int q = 0;"),
+    # the Q4 x Q8 integer path
+    "q8_round_half_even": ("c = roundf(t); /* halves away from zero */",
+                           "c = rintf(t); /* halves away from zero */"),
+    "q8_scale_255": ("float db = amax / 127.0f;", "float db = amax / 255.0f;"),
+    "q8_no_offset": ("isum += (int64_t)(lo - 8) * q[32 * b + j];",
+                     "isum += (int64_t)lo * q[32 * b + j];"),
+    "q8_nibble_order": ("int lo = blk[2 + j] & 0x0F, hi = blk[2 + j] >> 4;",
+                        "int hi = blk[2 + j] & 0x0F, lo = blk[2 + j] >> 4;"),
+    "q8_signed_max": ("float a = fabsf(xb[j]);", "float a = xb[j];"),
     "f64_rounds_x": ("double p = (double)wrow[kk] * x[kk];",
                      "double p = (double)wrow[kk] * (double)(float)x[kk];"),
 }
@@ -60,6 +69,7 @@ def test_pins_catch_planted_mistake(tmp_path, name):
                         ignore=shutil.ignore_patterns("*.so", "__pycache__", "*.tmp*"))
     (tmp_path / "oracle" / "q4_oracle.c").write_text(src.replace(before, after))
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
-                        "tests/test_oracle_pins.py", "tests/test_oracle_pins_glue.py"],
+                        "tests/test_oracle_pins.py", "tests/test_oracle_pins_glue.py",
+                        "tests/test_oracle_pins_q8.py"],
                        cwd=tmp_path, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"mutant {name} passed every pin:\n{r.stdout[-2000:]}"
