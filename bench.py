@@ -431,7 +431,7 @@ def _run_single_gemv(args, dev, stream, hbm, torch):
     out = {"workload": "single Q4_0 GEMV 4096x3072, batch 1, fp32 x and y",
            "algorithmic_bytes_per_call": algo,
            "l2": f"{copies} weight copies rotated ({copies * n * k // 32 * 18 / 1e6:.0f} MB)"}
-    from bit_weight_quantized_03_b300 import q4_gemv_r, q4_repack
+    from bit_weight_quantized_03_b300 import q4_gemv_q8, q4_gemv_r, q4_repack
     Rs = [q4_repack(W, n, k) for W in Ws]
     wsr = Workspace(dev)
     calls = {
@@ -440,6 +440,8 @@ def _run_single_gemv(args, dev, stream, hbm, torch):
         "q4_gemv": lambda i: q4_gemv(Ws[i % copies], n, k, x, y=y, workspace=ws, stream=stream),
         "q4_gemv_r": lambda i: q4_gemv_r(Rs[i % copies], n, k, x, y=y, workspace=wsr,
                                          stream=stream),
+        # the Q4 x Q8 integer path (x quantized per 32 inside the kernel)
+        "q4_gemv_q8": lambda i: q4_gemv_q8(Ws[i % copies], n, k, x, y=y[0], stream=stream),
     }
     for name, call in calls.items():
         with torch.cuda.stream(stream):
@@ -455,7 +457,9 @@ def _run_single_gemv(args, dev, stream, hbm, torch):
         out[name] = {"us_per_call": us, "gbs": algo / (us * 1e-6) / 1e9,
                      "frac_of_hbm": algo / (us * 1e-6) / 1e9 / hbm}
         del g
-    best = min((v["us_per_call"], key) for key, v in out.items() if isinstance(v, dict))
+    # the fastest fp32 path (the integer path computes a different product)
+    best = min((v["us_per_call"], key) for key, v in out.items()
+               if isinstance(v, dict) and key != "q4_gemv_q8")
     out["best"] = best[1]
     return out
 
@@ -515,8 +519,10 @@ def _run_head_gather(args, dev, stream, hbm, torch):
         Rt = q4_repack(table, V, H)
         wsr = Workspace(dev)
         am = torch.zeros(2, dtype=torch.int32, device=dev)
+        from bit_weight_quantized_03_b300 import q4_gemv_q8
         variants = {
             "q4_gemv_r": lambda: q4_gemv_r(Rt, V, H, xh, y=logits, workspace=wsr, stream=stream),
+            "q4_gemv_q8": lambda: q4_gemv_q8(table, V, H, xh, y=logits[0], stream=stream),
             "argmax_no_logits": lambda: q4_chain([Link(Rt, V, H, xh, argmax=am, ops=OP_ARGMAX)],
                                                  workspace=wsr, stream=stream),
         }
@@ -531,7 +537,7 @@ def _run_head_gather(args, dev, stream, hbm, torch):
             _time_graph_replays([(gv, 2)], stream, torch)
             vms = statistics.median(_time_graph_replays([(gv, 1)], stream, torch)
                                     for _ in range(5)) / reps
-            algo = head_bytes + 4 * H + (4 * V if name == "q4_gemv_r" else 8)
+            algo = head_bytes + 4 * H + (8 if name == "argmax_no_logits" else 4 * V)
             extra["head_gemv"][name] = {"us_per_call": vms * 1e3,
                                         "weight_gbs": head_bytes / (vms * 1e-3) / 1e9,
                                         "frac_of_hbm": algo / (vms * 1e-3) / 1e9 / hbm}
@@ -619,6 +625,61 @@ def _fp32_fma_peak(dev, stream, torch):
         torch.backends.cuda.matmul.allow_tf32 = prev
 
 
+CROSSOVER_SHAPES = [(4096, 3072), (1024, 3072), (3072, 4096), (9216, 3072), (3072, 9216),
+                    (3840, 1280), (1280, 1280), (5120, 1280), (1280, 5120)]
+
+
+def _crossover_by_shape(dev, stream, torch, ms=(1, 2, 3, 4, 5, 6, 8, 12, 16)):
+    """Per decoder and encoder shape: fp32 GEMV vs bf16 tensor-core GEMM time at
+    each M the GEMV takes, L2-cold (weight copies rotated, >= 256 MB), and the
+    largest M at which the GEMV is still faster for every M up to it (the
+    value q4_linear_crossover_m returns for that shape)."""
+    import synth
+    from bit_weight_quantized_03_b300 import FLAG_PDL, Workspace, q4_gemm, q4_gemv, q4_quantize
+    out = {}
+    for n, k in CROSSOVER_SHAPES:
+        wbytes = n * k // 32 * 18
+        copies = max(2, -(-(256 << 20) // wbytes))
+        Ws = []
+        for c in range(copies):
+            w = synth.torch_weights(n, k, seed=synth.seed_for(5, 1, c), device=dev)
+            Ws.append(q4_quantize(w))
+            del w
+        reps = max(copies, 24)
+        ws = Workspace(dev)
+        times = {}
+        for M in ms:
+            x32 = synth.torch_activations(M, k, seed=synth.activation_seed(5100, M), device=dev)
+            xbf = x32.to(torch.bfloat16)
+            y = torch.empty((M, n), device=dev)
+            t = {}
+            for name, fn in (("gemv", lambda W: q4_gemv(W, n, k, x32, y=y, workspace=ws,
+                                                        flags=FLAG_PDL, stream=stream)),
+                             ("gemm", lambda W: q4_gemm(W, n, k, xbf, Y=y, workspace=ws,
+                                                        flags=FLAG_PDL, stream=stream))):
+                with torch.cuda.stream(stream):
+                    fn(Ws[0])
+                    stream.synchronize()
+                    g = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(g, stream=stream):
+                        for i in range(reps):
+                            fn(Ws[i % copies])
+                _time_graph_replays([(g, 1)], stream, torch)
+                t[name] = statistics.median(_time_graph_replays([(g, 1)], stream, torch)
+                                            for _ in range(3)) / reps * 1e3
+                del g
+            times[str(M)] = {"gemv_us": t["gemv"], "gemm_us": t["gemm"]}
+        last = 0
+        for M in ms:
+            if times[str(M)]["gemv_us"] <= times[str(M)]["gemm_us"]:
+                last = M
+            else:
+                break
+        out[f"{n}x{k}"] = {"by_m": times, "gemv_up_to_m": last, "copies": copies}
+        del Ws
+    return out
+
+
 def _run_crossover(args, dev, stream, hbm, bf16_burst, torch):
     """Batched decode on the 4096x3072 decoder shape: fp32 GEMV vs bf16 tensor-core
     GEMM for M in 1..128 concurrent streams, L2-cold (72 weight copies, 510 MB)."""
@@ -669,9 +730,11 @@ def _run_crossover(args, dev, stream, hbm, bf16_burst, torch):
         if "gemv" not in r or r["gemm"]["us"] < r["gemv"]["us"]:
             cross = M
             break
+    del Ws
+    by_shape = _crossover_by_shape(dev, stream, torch)
     return {"workload": "batched decode, 4096x3072 Q4_0, M concurrent streams, fp32 x (GEMV) / "
                         "bf16 x (tensor-core GEMM), fp32 y; 72 weight copies rotated (L2-cold)",
-            "by_m": rows, "crossover_m": cross,
+            "by_m": rows, "crossover_m": cross, "by_shape": by_shape,
             "fp32_peak_tflops": {"value": fp32_peak,
                                  "source": "cuBLAS SGEMM 8192^3, TF32 off, measured in this run"},
             "note": "crossover_m = smallest M at which the tensor-core GEMM is faster; "

@@ -26,7 +26,7 @@ __all__ = [
     "q4_gemv_workspace_bytes", "q4_gemm_workspace_bytes", "q4_linear_workspace_bytes",
     "q4_linear_crossover_m", "Workspace", "Q4Error", "lib", "packed_bytes",
     "q4_repack", "q4_repack_bytes", "q4_chain", "q4_chain_workspace_bytes", "q4_gemv_r",
-    "q4_gemv_r_workspace_bytes", "Link", "LinkOut", "interleave_gate_rows",
+    "q4_gemv_r_workspace_bytes", "Link", "LinkOut", "interleave_gate_rows", "q4_gemv_q8",
 ]
 
 
@@ -172,6 +172,18 @@ def q4_gemv_noalloc(W, n: int, k: int, x, y=None, status=None, flags: int = 0, s
     ldy = _row_stride(y, "y")
     check(lib().q4_gemv_noalloc(_ptr(W), n, k, _ptr(x), m, ldx, _ptr(y), ldy, _ptr(status),
                                 flags, _stream(stream)), "q4_gemv_noalloc")
+    return y
+
+
+def q4_gemv_q8(W, n: int, k: int, x, y=None, stream=None):
+    """y [n] = W x on the integer path: x [k] (or [1, k]) fp32 quantized per 32
+    to int8 inside the kernel, exact integer block sums."""
+    torch = _torch()
+    if x.numel() != k or not x.is_contiguous():
+        raise ValueError("x must be a contiguous vector of k elements")
+    if y is None:
+        y = torch.empty((n,), dtype=torch.float32, device=x.device)
+    check(lib().q4_gemv_q8(_ptr(W), n, k, _ptr(x), _ptr(y), _stream(stream)), "q4_gemv_q8")
     return y
 
 

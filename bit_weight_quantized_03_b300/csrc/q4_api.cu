@@ -251,16 +251,34 @@ q4_status q4_gemv_chain(const q4_gemv_stage* stages, int32_t n_stages, void* wor
 }
 
 int64_t q4_linear_crossover_m(int64_t n, int64_t k) {
-  (void)n;
-  // Largest batch still sent to the fp32 GEMV.  Measured on B300 on the
-  // 4096 x 3072 decoder shape (L2-cold, CUDA graphs): the GEMV takes 5.1 /
-  // 7.2 / 9.9 us for 1 / 2 / 4 rows of x (one launch of the batched tile
-  // kernel up to 4 rows), the split-K tensor-core GEMM 13.5-13.7 us for
-  // M = 1..4 and 14.8 us at M = 8, where the GEMV needs two launches (19.4 us);
-  // at M = 5..7 a 4-row launch plus the rest already costs more than the GEMM.
   // The tensor-core path needs k % 256 == 0.
-  if (k % 256 != 0) return Q4_GEMV_MAX_M;
-  return 4;
+  if (n <= 0 || k <= 0 || k % 256 != 0) return Q4_GEMV_MAX_M;
+  // Largest batch still sent to the fp32 GEMV, measured on B300 per decoder
+  // and encoder shape (L2-cold weight copies, CUDA graphs): the smallest M in
+  // {1..6, 8, 12, 16} at which the bf16 tensor-core GEMM beat the GEMV, less
+  // one step.  The GEMV reads the weights once per 4 rows of x, so its time
+  // steps up after M = 4, 8, ...; the GEMM's stays ~flat over this range.
+  struct Entry {
+    int64_t n, k, m;
+  };
+  static const Entry kTable[] = {
+      {4096, 3072, 4}, {1024, 3072, 6}, {3072, 4096, 4}, {9216, 3072, 6}, {3072, 9216, 4},
+      {3840, 1280, 8}, {1280, 1280, 6}, {5120, 1280, 8}, {1280, 5120, 6},
+  };
+  // exact shape, else the entry nearest in weight count (log scale)
+  const double size = static_cast<double>(n) * static_cast<double>(k);
+  const Entry* best = &kTable[0];
+  double best_d = 1e300;
+  for (const Entry& e : kTable) {
+    if (e.n == n && e.k == k) return e.m;
+    const double r = size / (static_cast<double>(e.n) * static_cast<double>(e.k));
+    const double d = r > 1.0 ? r : 1.0 / r;
+    if (d < best_d) {
+      best_d = d;
+      best = &e;
+    }
+  }
+  return best->m;
 }
 
 size_t q4_linear_workspace_bytes(int64_t n, int64_t k, int64_t m, q4_dtype x_dtype) {

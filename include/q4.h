@@ -205,6 +205,23 @@ size_t q4_gemm_workspace_bytes(int64_t n, int64_t k, int64_t m);
 q4_status q4_embed_gather(const void* table, int64_t vocab, int64_t k, const int32_t* ids,
                           int64_t n_ids, float* out, int32_t* status_dev, q4_stream_t s);
 
+/* Batch-1 product on the integer path: y = W x with x quantized per 32
+ * elements to int8 (GGUF Q4_0's usual companion; the pages, "Arquitectura",
+ * name only the weight format, so the reading is this library's): per block
+ * amax = max |x_j|, d_x = amax / 127 (fp32, IEEE division), q_x = x / d_x
+ * rounded to nearest with halves away from zero (IEEE division); amax == 0
+ * gives d_x = +0 and codes 0, a NaN or infinity in the block gives d_x = NaN
+ * (so every output is NaN).  Each block adds d_w * d_x * sum (q_w - 8) q_x
+ * with the integer sum exact; y is within 1e-4 * sum_b |block term| of the fp64
+ * value of that sum, and within sum_j |w^_j| d_x,b(j) / 2 more of the product
+ * with the unquantized x.
+ *   W  GGUF Q4_0 [n rows of k/32 blocks], 16-byte aligned; k % 32 == 0,
+ *      k <= 12288 (else Q4_ERR_UNSUPPORTED_SHAPE).
+ *   x  fp32 [k], 4-byte aligned;  y  fp32 [n], 4-byte aligned.
+ * No workspace; results do not depend on timing. */
+q4_status q4_gemv_q8(const void* W, int64_t n, int64_t k, const float* x, float* y,
+                     q4_stream_t s);
+
 /* ---------------------------------------------------------------------------
  * Repacked layout and the decode-step chain.
  *
@@ -315,6 +332,11 @@ q4_status q4_linear(const void* W, int64_t n, int64_t k, const void* X, q4_dtype
                     int64_t ldx, float* Y, int64_t ldy, void* workspace, size_t ws_bytes,
                     int32_t* status_dev, uint32_t flags, q4_stream_t s);
 size_t q4_linear_workspace_bytes(int64_t n, int64_t k, int64_t m, q4_dtype x_dtype);
+/* The largest m that q4_linear sends to the fp32 GEMV: a table measured on
+ * B300 for the decoder shapes (4096x3072, 1024x3072, 3072x4096, 9216x3072,
+ * 3072x9216) and the encoder shapes (3840x1280, 1280x1280, 5120x1280,
+ * 1280x5120); another shape takes the entry nearest to it in weight count;
+ * k % 256 != 0 (no tensor-core path) gives Q4_GEMV_MAX_M. */
 int64_t q4_linear_crossover_m(int64_t n, int64_t k);
 
 /* Static strings; never NULL. */

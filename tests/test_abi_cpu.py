@@ -140,6 +140,17 @@ def _bad_link(q4, **kw):
     return arr
 
 
+def test_gemv_q8_host_validation(q4):
+    L = q4.lib()
+    A16 = 1 << 20  # a 16-byte-aligned fake address: nothing is launched on these paths
+    assert L.q4_gemv_q8(None, 4, 64, A16, A16, None) == q4.ERR_INVALID_ARG
+    assert L.q4_gemv_q8(A16, 0, 64, A16, A16, None) == q4.ERR_INVALID_ARG
+    assert L.q4_gemv_q8(A16, 4, 48, A16, A16, None) == q4.ERR_UNSUPPORTED_SHAPE
+    assert L.q4_gemv_q8(A16, 4, 12288 + 32, A16, A16, None) == q4.ERR_UNSUPPORTED_SHAPE
+    assert L.q4_gemv_q8(A16 + 2, 4, 64, A16, A16, None) == q4.ERR_MISALIGNED
+    assert L.q4_gemv_q8(A16, 4, 64, A16 + 2, A16, None) == q4.ERR_MISALIGNED
+
+
 def test_repacked_and_chain_host_validation(q4):
     L = q4.lib()
     assert L.q4_repack_bytes(4, 288) == 0

@@ -368,3 +368,31 @@ def test_config5_crossover_shapes(torch, q4, oracle_mod, m):
     Y, S = oracle_mod.matmul(W, n, k, xb.float().numpy(), nthreads=oracle_mod.cpu_count())
     ok, info = within_tol(yg, Y, S, GEMM_TOL)
     assert ok, info
+
+
+# the measured crossover table of q4_linear (largest M sent to the fp32 GEMV)
+CROSSOVER = {(4096, 3072): 4, (1024, 3072): 6, (3072, 4096): 4, (9216, 3072): 6,
+             (3072, 9216): 4, (3840, 1280): 8, (1280, 1280): 6, (5120, 1280): 8,
+             (1280, 5120): 6}
+
+
+@pytest.mark.parametrize("shape", sorted(CROSSOVER))
+def test_linear_at_each_shapes_crossover(torch, q4, oracle_mod, shape):
+    """q4_linear at the measured crossover of every decoder and encoder shape
+    and one row either side: the path it takes (fp32 GEMV up to the
+    crossover, bf16 tensor-core GEMM past it) is checked element-wise against
+    the oracle with that path's tolerance."""
+    n, k = shape
+    c = CROSSOVER[shape]
+    assert q4.q4_linear_crossover_m(n, k) == c
+    W, rc, _ = oracle_mod.quantize(synth.np_weights(n, k, seed=synth.seed_for(5, 2, n + k)))
+    assert rc == 0
+    Wd = torch.from_numpy(W).cuda()
+    for m in (c - 1, c, c + 1):
+        x = synth.np_activations(m, k, seed=synth.activation_seed(5200 + n + k, m))
+        y = q4.q4_linear(Wd, n, k, torch.from_numpy(x).cuda()).cpu().numpy()
+        gemv = m <= c
+        Y, S = oracle_mod.matmul(W, n, k, x if gemv else bf16_round(x),
+                                 nthreads=oracle_mod.cpu_count())
+        ok, info = within_tol(y, Y, S, GEMV_TOL if gemv else GEMM_TOL)
+        assert ok, (shape, m, info)
