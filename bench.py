@@ -295,6 +295,37 @@ def run_ours(args):
     return 0
 
 
+# DRAM bytes (read + write) per decode step from ncu captures of the kernels
+# as they stand (profiles/decode_step_dram_traffic.md): a 2-layer step
+# captured, scaled to 26 layers (every layer has the same four shapes, so the
+# traffic grows with the layer count).  Each entry is used only while the
+# kernel sources hash to what they were when captured, else it is null.
+STEP_TRAFFIC = {
+    "per_launch": {"bytes_per_step": 26 * 65_985_280,
+                   "sources": ("q4_gemv_b1.cu", "q4_gemv_tile.cuh"),
+                   "sha16": "2818c95998691340"},
+    "fused": {"bytes_per_step": 13 * 135_205_376,
+              "sources": ("q4_chain.cu", "q4r_tile.cuh"),
+              "sha16": "5e9eade3da070177"},
+}
+
+
+def _sources_sha16(names):
+    import hashlib
+    h = hashlib.sha256()
+    for nm in names:
+        with open(os.path.join(ROOT, "bit_weight_quantized_03_b300", "csrc", nm), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _step_traffic(path):
+    t = STEP_TRAFFIC.get(path)
+    if t is None or _sources_sha16(t["sources"]) != t["sha16"]:
+        return None
+    return t["bytes_per_step"]
+
+
 def _run_stack(args, world, dev, stream, hbm, peak_src, torch):
     """Decoder linear stack at batch-1 decode (headline).  The step runs as one
     q4_gemv_chain launch (104 dependent products); the same step as 104 q4_gemv
@@ -302,7 +333,7 @@ def _run_stack(args, world, dev, stream, hbm, peak_src, torch):
     import synth
     from bit_weight_quantized_03_b300.stacks import DecoderStack
 
-    dec = DecoderStack(device=dev)
+    dec = DecoderStack(device=dev, **({} if args.layers is None else {"layers": args.layers}))
     wbytes = dec.weight_bytes()
     abytes = dec.activation_bytes()
     G = 8
@@ -342,6 +373,26 @@ def _run_stack(args, world, dev, stream, hbm, peak_src, torch):
     ms_step = ms / args.steps
     value = world * wbytes * args.steps / (ms * 1e-3) / 1e9
     achieved = (wbytes + abytes) / (ms_step * 1e-3) / 1e9
+
+    # ---------------- where the per-launch step's time goes: each kind of
+    # product (one per layer) timed as its own PDL chain
+    breakdown = {}
+    for key in ("qkv", "wo", "w13", "w2"):
+        gk = dec.capture_only(key, G, stream)
+        _time_graph_replays([(gk, 1)], stream, torch)
+        kms = statistics.median(_time_graph_replays([(gk, 1)], stream, torch)
+                                for _ in range(5)) / G
+        n_k, k_k = dec.shapes[key]
+        kbytes = dec.layers * (n_k * k_k // 32 * 18)
+        breakdown[key] = {"ms_per_step": kms, "launches": dec.layers,
+                          "us_per_launch": kms * 1e3 / dec.layers,
+                          "weight_gbs": kbytes / (kms * 1e-3) / 1e9}
+        del gk
+    breakdown["sum_ms"] = sum(v["ms_per_step"] for v in breakdown.values())
+    breakdown["note"] = ("each kind's products of a step timed as their own PDL chain of "
+                         "q4_gemv launches (CUDA events, graphs of 8 steps); their sum against "
+                         "step_paths.per_launch.ms_per_step shows what running the four kinds "
+                         "back to back adds or saves")
 
     # ---------------- e2e: host input -> step -> host output, every step
     rows = max(args.steps, 3)  # the 3 untimed warm-up steps use rows 0..2 too
@@ -393,7 +444,12 @@ def _run_stack(args, world, dev, stream, hbm, peak_src, torch):
                    "step_function": STEP_FUNCTION[best],
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "traffic": args.traffic,
+                     "frac": achieved / hbm,
+                     "traffic": (args.traffic if args.traffic is not None else
+                                 (_step_traffic(best) if dec.layers == 26 else None)),
+                     "traffic_note": ("DRAM read + write bytes per step (ncu, a 2-layer step "
+                                      "scaled to 26 layers); algorithmic bytes per step "
+                                      f"{wbytes + abytes}"),
                      "kernel": KERNELS[best],
                      "peak_source": f"{peak_src} HBM copy bandwidth",
                      "per_launch": ("algorithmic bytes of the 104 launches of a step / step time "
@@ -406,6 +462,7 @@ def _run_stack(args, world, dev, stream, hbm, peak_src, torch):
                            "regions": v[1]["regions"], "note": PATH_NOTES[k],
                            "step_function": STEP_FUNCTION[k]}
                        for k, v in paths.items()},
+        "per_launch_breakdown": breakdown,
         "e2e": e2e,
         "gpu_launches": args.steps * (dec.launches_per_step() if best == "per_launch" else 1),
         "clocks": clocks,
@@ -753,6 +810,8 @@ def main():
                     default="all",
                     help="run one section (profiling runs); the default runs all of them")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--layers", type=int, default=None,
+                    help="decoder layers of the stack (default 26; fewer only for profiling)")
     ap.add_argument("--traffic", type=float, default=None,
                     help="per-launch DRAM bytes of the GEMV kernel from an ncu capture")
     args = ap.parse_args()

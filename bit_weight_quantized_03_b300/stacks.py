@@ -122,6 +122,29 @@ class DecoderStack:
         q4_gemv(W["w2"], h, self.FFN, self.y_13[:, :self.FFN], y=self.x, workspace=self.ws,
                 flags=FLAG_PDL, stream=stream)
 
+    def step_only(self, key, stream=None):
+        """The products of one kind ("qkv", "wo", "w13" or "w2") of a decode step,
+        one per layer, as their own chain of q4_gemv launches with programmatic
+        dependent launch: timing these apart shows where a step's time goes."""
+        n, k = self.shapes[key]
+        src = {"qkv": self.x, "wo": self.y_qkv[:, :self.QDIM], "w13": self.y_o,
+               "w2": self.y_13[:, :self.FFN]}[key]
+        dst = {"qkv": self.y_qkv, "wo": self.y_o, "w13": self.y_13, "w2": self.x}[key]
+        for l in range(self.layers):
+            q4_gemv(self.W[l][key], n, k, src, y=dst, workspace=self.ws, flags=FLAG_PDL,
+                    stream=stream)
+
+    def capture_only(self, key, steps, stream):
+        torch = self.torch
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            self.step_only(key, stream)
+            stream.synchronize()
+            with torch.cuda.graph(g, stream=stream):
+                for _ in range(steps):
+                    self.step_only(key, stream)
+        return g
+
     def links(self, x_in):
         """The step's 104 products as chain links (W, n, k, x, y), in order."""
         H, Q, F = self.HIDDEN, self.QDIM, self.FFN
@@ -336,3 +359,52 @@ class AdapterStack:
                 for _ in range(passes):
                     self.forward(X_enc, stream)
         return g
+
+
+def _main(argv=None):
+    """Run a few steps of a stack with no timing, for a profiler:
+        python -m bit_weight_quantized_03_b300.stacks decode --layers 2 --path fused --steps 4
+        python -m bit_weight_quantized_03_b300.stacks head --steps 3
+    decode runs the decoder step on its per-launch (q4_gemv), chain
+    (q4_gemv_chain) or fused (q4_chain, repacked) path; head runs the
+    131072 x 3072 output head once per step as q4_gemv_r (repacked) and as
+    q4_gemv (GGUF)."""
+    import argparse
+
+    import torch
+    ap = argparse.ArgumentParser(prog="python -m bit_weight_quantized_03_b300.stacks")
+    ap.add_argument("what", choices=["decode", "head"])
+    ap.add_argument("--layers", type=int, default=synth.DECODER_LAYERS)
+    ap.add_argument("--path", choices=["per_launch", "chain", "fused"], default="fused")
+    ap.add_argument("--steps", type=int, default=3)
+    a = ap.parse_args(argv)
+    dev = torch.device("cuda", 0)
+    if a.what == "decode":
+        dec = DecoderStack(layers=a.layers, device=dev)
+        x = synth.torch_activations(1, 3072, seed=synth.activation_seed(2000), device=dev)
+        for _ in range(a.steps):
+            if a.path == "fused":
+                dec.fused_step(x)
+            else:
+                dec.step(x, chain=a.path == "chain")
+    else:
+        from . import q4_gemv_r
+        V, H = synth.VOCAB, 3072
+        table = torch.empty((V, H // 32 * 18), dtype=torch.uint8, device=dev)
+        for r0 in range(0, V, 16384):
+            w = synth.torch_weights(16384, H, seed=synth.seed_for(3, 0, r0 // 16384), device=dev)
+            q4_quantize(w, blocks=table[r0:r0 + 16384])
+            del w
+        R = q4_repack(table, V, H)
+        x = synth.torch_activations(1, H, seed=synth.activation_seed(3000), device=dev)
+        y = torch.empty((1, V), device=dev)
+        ws, wsr = Workspace(dev), Workspace(dev)
+        for _ in range(a.steps):
+            q4_gemv_r(R, V, H, x, y=y, workspace=wsr)
+            q4_gemv(table, V, H, x, y=y, workspace=ws)
+    torch.cuda.synchronize()
+    print("ok")
+
+
+if __name__ == "__main__":
+    _main()
