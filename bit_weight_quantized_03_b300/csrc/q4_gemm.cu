@@ -430,14 +430,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++wj;
         // k-steps 4j + p and 4j + p + 2 (blocks 2p, 2p + 1 and 2p + 4, 2p + 5 of
         // the run) go to A stage p
+        // The k-step is decoded before waiting for its A stage, so that only
+        // the TMEM store sits between the MMA that frees the stage and the
+        // MMA that reads it next.
         auto one_kstep = [&](auto kk_tag) -> bool {
           constexpr int KK = decltype(kk_tag)::value;
-          const bool free_stage = mbar_wait(B.a_empty + 8 * p, (a_use & 1) ^ 1, abort_flag);
-          if (!__all_sync(0xffffffffu, free_stage)) return false;
-          tc_fence_after();
           uint32_t o[32];
           decode_block_bf16<2 * KK>(r, dc, o);
           decode_block_bf16<2 * KK + 1>(r, dc, o + 16);
+          const bool free_stage = mbar_wait(B.a_empty + 8 * p, (a_use & 1) ^ 1, abort_flag);
+          if (!__all_sync(0xffffffffu, free_stage)) return false;
+          tc_fence_after();
           tmem_st32(lane_addr + a_col(p), o);
           tmem_st_wait();
           tc_fence_before();
