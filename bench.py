@@ -497,6 +497,8 @@ def _run_single_gemv(args, dev, stream, hbm, torch):
         "q4_gemv": lambda i: q4_gemv(Ws[i % copies], n, k, x, y=y, workspace=ws, stream=stream),
         "q4_gemv_r": lambda i: q4_gemv_r(Rs[i % copies], n, k, x, y=y, workspace=wsr,
                                          stream=stream),
+        "q4_gemv_r_pdl": lambda i: q4_gemv_r(Rs[i % copies], n, k, x, y=y, workspace=wsr,
+                                             flags=FLAG_PDL, stream=stream),
         # the Q4 x Q8 integer path (x quantized per 32 inside the kernel)
         "q4_gemv_q8": lambda i: q4_gemv_q8(Ws[i % copies], n, k, x, y=y[0], stream=stream),
     }

@@ -196,9 +196,11 @@ __device__ __forceinline__ void group_owners(const SLink& S, int g, uint32_t C, 
   }
 }
 
+// Warp w's share [a, b) of a CTA's tiles [ca, cb) when NW warps split them.
+template <int NW>
 __device__ __forceinline__ void warp_range(int ca, int cb, int w, int& a, int& b) {
-  a = ca + (cb - ca) * w / kWarps;
-  b = ca + (cb - ca) * (w + 1) / kWarps;
+  a = ca + (cb - ca) * w / NW;
+  b = ca + (cb - ca) * (w + 1) / NW;
 }
 
 // What a thread carries around for bounded waits.
@@ -331,18 +333,20 @@ __device__ __forceinline__ bool load_entries(const Ent (&en)[W], Ctx& x, float4 
 
 // The element quad that lane `lane` of warp `warp` stages as its m-th in pass
 // `pass`: warp w stages slice 16 pass + w, two quads per lane.
+template <int NW>
 __device__ __forceinline__ int stage_quad(int pass, int warp, int lane, int m) {
-  return 64 * (pass * kWarps + warp) + 32 * m + lane;
+  return 64 * (pass * NW + warp) + 32 * m + lane;
 }
 
 // The x entries of staging pass `pass`.
+template <int NW>
 __device__ __forceinline__ void x_entries(const SLink* sl, float* set_base, const SLink& S,
                                           int pass, int tid, uint32_t C,
                                           Ent (&en)[kStageQuads + 1]) {
   const int quads = S.k / 4;
 #pragma unroll
   for (int m = 0; m < kStageQuads; ++m) {
-    const int q = stage_quad(pass, tid >> 5, tid & 31, m);
+    const int q = stage_quad<NW>(pass, tid >> 5, tid & 31, m);
     en[m].np = -1;
     if (q < quads) en[m] = make_entry(sl, set_base, S.ext[0], S.src_link[0], S.src_off[0] + 4 * q, C);
   }
@@ -354,6 +358,7 @@ __device__ __forceinline__ float silu_gate(float a, float b) { return a / (1.0f 
 // quads per lane) scaled by a power of two and split into binary16 hi + lo
 // (q4r_tile.cuh layout), its inverse scale in xinv[slice].  A warp's quads
 // are all valid or all past k (k % 256 == 0).
+template <int NW>
 __device__ __forceinline__ void convert_x(const float4 (&v)[kStageQuads + 1],
                                           const Ent (&en)[kStageQuads + 1], int pass, int tid,
                                           uint8_t* x16, float* xinv) {
@@ -371,7 +376,7 @@ __device__ __forceinline__ void convert_x(const float4 (&v)[kStageQuads + 1],
 #pragma unroll
   for (int m = 0; m < kStageQuads; ++m) {
     if (en[m].np < 0) continue;
-    const int e = 4 * stage_quad(pass, warp, lane, m);
+    const int e = 4 * stage_quad<NW>(pass, warp, lane, m);
     __half h[4], l[4];
     rt::split_hi_lo(v[m].x * sc, h[0], l[0]);
     rt::split_hi_lo(v[m].y * sc, h[1], l[1]);
@@ -412,20 +417,23 @@ struct TileStream {
   const uint8_t* psrc;
 };
 
+template <int NW>
 __device__ __forceinline__ void stream_enter(const SLink* sl, TileStream& ts, int warp) {
   const SLink& L = sl[ts.ps];
   int a, b;
-  warp_range(L.ca, L.cb, warp, a, b);
+  warp_range<NW>(L.ca, L.cb, warp, a, b);
   ts.left = b - a;
   ts.psrc = L.R + static_cast<size_t>(a) * rt::kTileBytes;
 }
 
+template <int NW>
 __device__ __forceinline__ void stream_settle(const SLink* sl, int n_links, TileStream& ts,
                                               int warp) {
   while (ts.ps < n_links && ts.left == 0)
-    if (++ts.ps < n_links) stream_enter(sl, ts, warp);
+    if (++ts.ps < n_links) stream_enter<NW>(sl, ts, warp);
 }
 
+template <int NW>
 __device__ __forceinline__ void stream_issue(const SLink* sl, int n_links, TileStream& ts,
                                              int warp, int lane, uint32_t ring, uint32_t bar0,
                                              uint64_t pol) {
@@ -439,13 +447,14 @@ __device__ __forceinline__ void stream_issue(const SLink* sl, int n_links, TileS
   ++ts.issued;
   ts.psrc += nt * rt::kTileBytes;
   ts.left -= nt;
-  if (ts.left == 0) stream_settle(sl, n_links, ts, warp);
+  if (ts.left == 0) stream_settle<NW>(sl, n_links, ts, warp);
 }
 
 // This warp's tiles [wa, wb) of the current link (g0w = wa / nsb): each
 // 16-row group's row products end in Pw[group - g0w][row].  Kept out of line
 // so that the decode loop is register-allocated on its own (inlined, the
 // staging code's live values cost it spills).
+template <int NW>
 __device__ __noinline__ bool run_tiles(const SLink* sl, int n_links, TileStream& tsr, Ctx& x,
                                           int warp, int lane, const uint8_t* ring_p,
                                           uint32_t ring, uint32_t bar0, const uint8_t* x16,
@@ -493,7 +502,7 @@ __device__ __noinline__ bool run_tiles(const SLink* sl, int n_links, TileStream&
     __syncwarp();
     fence_proxy_async_smem();
     ++ts.consumed;
-    stream_issue(sl, n_links, ts, warp, lane, ring, bar0, pol);
+    stream_issue<NW>(sl, n_links, ts, warp, lane, ring, bar0, pol);
   }
   if (ok && cur >= 0) flush(cur);
   tsr = ts;
@@ -579,10 +588,10 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
   ts.ps = 0;
   ts.issued = 0;
   ts.consumed = 0;
-  stream_enter(s_links, ts, warp);
-  stream_settle(s_links, n_links, ts, warp);
+  stream_enter<kWarps>(s_links, ts, warp);
+  stream_settle<kWarps>(s_links, n_links, ts, warp);
   for (int i = 0; i < kSlots; ++i)
-    stream_issue(s_links, n_links, ts, warp, lane, ring, bar0, pol);
+    stream_issue<kWarps>(s_links, n_links, ts, warp, lane, ring, bar0, pol);
 
   // ---- slot sets: a fresh workspace (or one last used with a smaller chain)
   // gets both sets reset before anyone publishes; otherwise the set of the
@@ -647,7 +656,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
       if (S.ops & kOpResidual) need = max(need, S.src_link[1]);
       if (lane == 0) {
         int a, b;
-        warp_range(S.ca, S.cb, warp, a, b);
+        warp_range<kWarps>(S.ca, S.cb, warp, a, b);
         s_wa[warp] = a;
         s_wb[warp] = b;
         s_wg[warp] = a < b ? make_int2(static_cast<int>(divq(static_cast<uint32_t>(a), S.divNsb)),
@@ -655,7 +664,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
                            : make_int2(1, 0);
       }
       if (S.gcount > 0) {
-        x_entries(s_links, set_base, S, 0, tid, x.C, en);
+        x_entries<kWarps>(s_links, set_base, S, 0, tid, x.C, en);
         // the residual rows of the groups this CTA holds the first tile of
         if ((S.ops & kOpResidual) && tid < S.gcount * 4) {
           const int g = S.g0c + tid / 4, row = 16 * g + 4 * (tid & 3);
@@ -721,23 +730,23 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
       float4 v[kStageQuads + 1];
       bool ok = load_entries(en, x, v);
       if (ok) {
-        convert_x(v, en, 0, tid, x16, xinv);
+        convert_x<kWarps>(v, en, 0, tid, x16, xinv);
         if (en[kStageQuads].np >= 0)
           *reinterpret_cast<float4*>(&sres[tid / 4][4 * (tid & 3)]) = v[kStageQuads];
       }
       for (int pass = 1; ok && pass * kWarps * 256 < S.k; ++pass) {
-        x_entries(s_links, set_base, S, pass, tid, x.C, en);
+        x_entries<kWarps>(s_links, set_base, S, pass, tid, x.C, en);
         en[kStageQuads].np = -1;
         ok = load_entries(en, x, v);
-        if (ok) convert_x(v, en, pass, tid, x16, xinv);
+        if (ok) convert_x<kWarps>(v, en, pass, tid, x16, xinv);
       }
     }
     stop = __syncthreads_or(*abort_flag) != 0;
     if (stop) break;
 
     // ---------------- this warp's tiles of link s
-    run_tiles(s_links, n_links, ts, x, warp, lane, ring_p, ring, bar0, x16, xinv, s_wa[warp],
-              s_wb[warp], s_wg[warp].x, S.nsb, P[warp]);
+    run_tiles<kWarps>(s_links, n_links, ts, x, warp, lane, ring_p, ring, bar0, x16, xinv,
+                      s_wa[warp], s_wb[warp], s_wg[warp].x, S.nsb, P[warp]);
     stop = __syncthreads_or(*abort_flag) != 0;
     if (stop) break;
 
@@ -884,16 +893,20 @@ struct SingleArgs {
   uint32_t ops, flags;
 };
 
-__global__ void __launch_bounds__(kThreads, 1) single_kernel(const SingleArgs a) {
+// NW = 16: one CTA per SM (a call alone).  NW = 8: half the warps and shared
+// memory, so that under programmatic dependent launch the next call's CTA fits
+// beside this one, fills its ring and only then waits for this call to end.
+template <int NW>
+__global__ void __launch_bounds__(NW * 32, 16 / NW) single_kernel(const SingleArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ __align__(8) uint64_t full_bar[kWarps][kSlots];
+  __shared__ __align__(8) uint64_t full_bar[NW][kSlots];
   __shared__ __align__(8) uint64_t never_bar;
-  __shared__ __align__(16) float P[kWarps][kWarpGroups][kSlotFloats];
+  __shared__ __align__(16) float P[NW][kWarpGroups][kSlotFloats];
   __shared__ __align__(16) SLink s_link[1];
-  __shared__ int s_wa[kWarps], s_wb[kWarps];
-  __shared__ int2 s_wg[kWarps];
-  __shared__ float s_bv[kWarps];
-  __shared__ int s_bi[kWarps];
+  __shared__ int s_wa[NW], s_wb[NW];
+  __shared__ int2 s_wg[NW];
+  __shared__ float s_bv[NW];
+  __shared__ int s_bi[NW];
   __shared__ int s_abort, s_last;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -906,7 +919,7 @@ __global__ void __launch_bounds__(kThreads, 1) single_kernel(const SingleArgs a)
   x.status = a.status;
   uint8_t* const ring_p = smem + warp * kSlots * kChunkBytes;
   const uint32_t ring = smem_u32(ring_p);
-  uint8_t* const x16 = smem + kWarps * kSlots * kChunkBytes;
+  uint8_t* const x16 = smem + NW * kSlots * kChunkBytes;
   float* const xinv = reinterpret_cast<float*>(x16 + rt::x16_bytes(a.k));
   const uint32_t bar0 = smem_u32(&full_bar[warp][0]);
   const uint64_t pol = l2_evict_first_policy();
@@ -929,7 +942,7 @@ __global__ void __launch_bounds__(kThreads, 1) single_kernel(const SingleArgs a)
   if (lane == 0) {
     for (int i = 0; i < kSlots; ++i) mbar_init(bar0 + 8 * i, 1);
     int wa, wb;
-    warp_range(ca, cb, warp, wa, wb);
+    warp_range<NW>(ca, cb, warp, wa, wb);
     s_wa[warp] = wa;
     s_wb[warp] = wb;
     s_wg[warp] = wa < wb ? make_int2(wa / a.nsb, (wb - 1) / a.nsb) : make_int2(1, 0);
@@ -940,9 +953,13 @@ __global__ void __launch_bounds__(kThreads, 1) single_kernel(const SingleArgs a)
   ts.ps = 0;
   ts.issued = 0;
   ts.consumed = 0;
-  stream_enter(s_link, ts, warp);
-  stream_settle(s_link, 1, ts, warp);
-  for (int i = 0; i < kSlots; ++i) stream_issue(s_link, 1, ts, warp, lane, ring, bar0, pol);
+  pdl_allow_dependents();
+  stream_enter<NW>(s_link, ts, warp);
+  stream_settle<NW>(s_link, 1, ts, warp);
+  for (int i = 0; i < kSlots; ++i) stream_issue<NW>(s_link, 1, ts, warp, lane, ring, bar0, pol);
+  // under programmatic dependent launch, x (and the residual) may be the
+  // previous kernel's output: read only after it has finished
+  pdl_wait_prior_grid();
   volatile int* abort_flag = &s_abort;
   if ((a.flags & kFlagTestStallOneWait) != 0 && c == 0 && tid == 0)
     if (!mbar_wait(smem_u32(&never_bar), 0, &s_abort)) fail(x);
@@ -953,10 +970,10 @@ __global__ void __launch_bounds__(kThreads, 1) single_kernel(const SingleArgs a)
     Ent en[kStageQuads + 1];
     float4 v[kStageQuads + 1];
     en[kStageQuads].np = -1;
-    for (int pass = 0; pass * kWarps * 256 < a.k; ++pass) {
-      x_entries(s_link, nullptr, S, pass, tid, C, en);
+    for (int pass = 0; pass * NW * 256 < a.k; ++pass) {
+      x_entries<NW>(s_link, nullptr, S, pass, tid, C, en);
       load_entries(en, x, v);  // plain loads: nothing to wait for
-      convert_x(v, en, pass, tid, x16, xinv);
+      convert_x<NW>(v, en, pass, tid, x16, xinv);
     }
   }
   bool stop = __syncthreads_or(*abort_flag) != 0;
@@ -965,8 +982,8 @@ __global__ void __launch_bounds__(kThreads, 1) single_kernel(const SingleArgs a)
   float bv = 0.f;
   int bi = -1;
   if (!stop) {
-    run_tiles(s_link, 1, ts, x, warp, lane, ring_p, ring, bar0, x16, xinv, s_wa[warp], s_wb[warp],
-              s_wg[warp].x, a.nsb, P[warp]);
+    run_tiles<NW>(s_link, 1, ts, x, warp, lane, ring_p, ring, bar0, x16, xinv, s_wa[warp],
+                  s_wb[warp], s_wg[warp].x, a.nsb, P[warp]);
     stop = __syncthreads_or(*abort_flag) != 0;
   }
   if (!stop && (a.ops & kOpSwiglu)) {
@@ -974,7 +991,7 @@ __global__ void __launch_bounds__(kThreads, 1) single_kernel(const SingleArgs a)
       const int gl = idx >> 3, j = idx & 7, g = g0c + gl;
       float va = 0.f, vb = 0.f;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
+      for (int w = 0; w < NW; ++w) {
         const int2 r = s_wg[w];
         if (g >= r.x && g <= r.y) {
           va += P[w][g - r.x][j];
@@ -990,7 +1007,7 @@ __global__ void __launch_bounds__(kThreads, 1) single_kernel(const SingleArgs a)
       const int gl = idx >> 4, row16 = idx & 15, g = g0c + gl, row = 16 * g + row16;
       float sum = 0.f;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
+      for (int w = 0; w < NW; ++w) {
         const int2 r = s_wg[w];
         if (g >= r.x && g <= r.y) sum += P[w][g - r.x][row16];
       }
@@ -1012,7 +1029,7 @@ __global__ void __launch_bounds__(kThreads, 1) single_kernel(const SingleArgs a)
     if (tid == 0) {
       float v = 0.f;
       int i = -1;
-      for (int w = 0; w < kWarps; ++w)
+      for (int w = 0; w < NW; ++w)
         if (s_bi[w] >= 0) better(v, i, s_bv[w], s_bi[w]);
       uint32_t* rec = a.hdr + kHdrRecords + 2 * c;
       st_relaxed_u32(rec, __float_as_uint(i >= 0 ? v : 0.f));
@@ -1245,13 +1262,47 @@ cudaError_t chain_launch(ChainArgs& A, void* workspace, cudaStream_t s) {
 
 // One link (its sources are in memory): the one-product kernel, unless the
 // CTAs' whole-group shares do not fit its per-warp bookkeeping.
-bool single_fits(const q4_chain_link& l) {
+bool single_fits(const q4_chain_link& l, int nw) {
   const int64_t C = sm_count(), nsb = l.k / 256, groups = (l.n + 15) / 16;
   if (C > kMaxCtas) return false;
   const int64_t per_cta = (groups + C - 1) / C * nsb;
-  const int64_t per_warp = (per_cta + kWarps - 1) / kWarps;
+  const int64_t per_warp = (per_cta + nw - 1) / nw;
   return per_warp / nsb + 2 <= kWarpGroups;
 }
+
+size_t single_smem_bytes(int nw, int k) {
+  return static_cast<size_t>(nw) * kSlots * kChunkBytes + static_cast<size_t>(rt::x16_bytes(k)) +
+         static_cast<size_t>(k / 256) * 4;
+}
+
+template <int NW>
+cudaError_t single_launch_nw(const SingleArgs& a, bool pdl, cudaStream_t s) {
+  static bool configured[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(single_kernel<NW>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(single_smem_bytes(NW, kMaxK)));
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(sm_count()));
+  cfg.blockDim = dim3(NW * 32);
+  cfg.dynamicSmemBytes = single_smem_bytes(NW, a.k);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, single_kernel<NW>, a);
+}
+
+// Alone: 16 warps, one CTA per SM.  With Q4_FLAG_PDL: the 8-warp shape when
+// its per-warp bookkeeping fits (two CTAs per SM), else the 16-warp one.
+bool single_usable(const q4_chain_link& l) { return single_fits(l, kWarps); }
 
 cudaError_t single_launch(const q4_chain_link& l, void* workspace, int32_t* status, uint32_t flags,
                           cudaStream_t s) {
@@ -1269,17 +1320,9 @@ cudaError_t single_launch(const q4_chain_link& l, void* workspace, int32_t* stat
   a.groups = static_cast<int32_t>((l.n + 15) / 16);
   a.ops = l.ops;
   a.flags = flags;
-  static bool configured[64] = {false};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(single_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(chain_smem_bytes(kMaxK)));
-    if (e != cudaSuccess) return e;
-    configured[dev] = true;
-  }
-  single_kernel<<<static_cast<unsigned>(sm_count()), kThreads, chain_smem_bytes(a.k), s>>>(a);
-  return cudaGetLastError();
+  const bool pdl = (flags & Q4_FLAG_PDL) != 0;
+  if (pdl && single_fits(l, 8)) return single_launch_nw<8>(a, true, s);
+  return single_launch_nw<kWarps>(a, pdl, s);
 }
 
 cudaError_t repack_launch(const uint8_t* W, int64_t n, int64_t k, uint8_t* R, cudaStream_t s) {
@@ -1329,7 +1372,7 @@ q4_status q4_chain(const q4_chain_link* links, int32_t n_links, void* workspace,
   A.status = status_dev;
   A.flags = flags;
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(s);
-  const cudaError_t e = (n_links == 1 && q4::single_fits(links[0]))
+  const cudaError_t e = (n_links == 1 && q4::single_usable(links[0]))
                             ? q4::single_launch(links[0], workspace, status_dev, flags, cs)
                             : q4::chain_launch(A, workspace, cs);
   return e == cudaSuccess ? Q4_OK : Q4_ERR_CUDA;

@@ -318,7 +318,11 @@ q4_status q4_chain(const q4_chain_link* links, int32_t n_links, void* workspace,
 /* Batch-1 product y = W x on a repacked matrix (a one-link q4_chain): the
  * per-token product of the decoder linears and the output head
  * ("Arquitectura").  Same error bound, workspace rules and x alignment as
- * q4_chain; y [n] fp32, 4-byte aligned. */
+ * q4_chain; y [n] fp32, 4-byte aligned.  A one-link chain is an ordinary
+ * launch (each CTA takes whole 16-row groups); with Q4_FLAG_PDL it is a
+ * programmatic dependent launch in a half-size CTA shape, so that two calls'
+ * CTAs share an SM and a call fills its weight ring while the previous kernel
+ * ends (x is read after that kernel). */
 size_t q4_gemv_r_workspace_bytes(int64_t n, int64_t k);
 q4_status q4_gemv_r(const void* R, int64_t n, int64_t k, const float* x, float* y,
                     void* workspace, size_t ws_bytes, int32_t* status_dev, uint32_t flags,

@@ -349,3 +349,43 @@ def test_chain_timeout_reports_and_recovers(torch, q4, oracle_mod):
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     _check_chain(oracle_mod, dec, x_np, [o.cpu().numpy() for o in outs], am.cpu().numpy())
+
+
+def test_gemv_r_pdl_dependent_calls_in_a_graph(torch, q4, oracle_mod):
+    """q4_gemv_r with Q4_FLAG_PDL (the half-size CTA shape, launched as a
+    programmatic dependent launch), captured in a CUDA graph as a chain of
+    dependent calls: y1 = A x, y2 = B y1, y3 = A' y2 ... each call's weights
+    are read before the previous call ends, its x only after.  Every output
+    element-wise against the oracle on the input that call read."""
+    shapes = [(512, 768), (256, 512), (1024, 256), (768, 1024)]
+    mats, Rs = [], []
+    for i, (n, k) in enumerate(shapes):
+        W = _quant(oracle_mod, n, k, 900 + i)
+        mats.append(W)
+        Rs.append(_repacked(torch, q4, W, n, k))
+    x0 = torch.from_numpy(synth.np_activations(1, 768, seed=901)).cuda()
+    ys = [torch.full((1, n), float("nan"), device="cuda") for n, _ in shapes]
+    ws = q4.Workspace()
+    s = torch.cuda.Stream()
+
+    def run():
+        src = x0
+        for (n, k), R, y in zip(shapes, Rs, ys):
+            q4.q4_gemv_r(R, n, k, src, y=y, workspace=ws, flags=q4.FLAG_PDL, stream=s)
+            src = y
+    with torch.cuda.stream(s):
+        run()
+        s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            run()
+        for y in ys:
+            y.fill_(float("nan"))
+        g.replay()
+    s.synchronize()
+    inp = x0.cpu().numpy()
+    for (n, k), W, y in zip(shapes, mats, ys):
+        got = y.cpu().numpy()
+        Y, S = oracle_mod.matmul(W, n, k, inp)
+        _check(got[0], Y[0], S[0], what=f"{n}x{k}")
+        inp = got
