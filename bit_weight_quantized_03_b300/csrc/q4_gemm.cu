@@ -317,7 +317,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer
-      int wj = 0, xk = 0;
+      // X ring slot and phase as running counters: a division by the runtime
+      // ring depth per k-step sits on this thread's critical path.
+      int wj = 0, xk = 0, xslot = 0;
+      uint32_t xph = 0;
       bool ok = true;
       for (int w = cta; w < args.tiles * args.splits && ok; w += ncta) {
         const Item it = item_of(w, args.splits, wstages);
@@ -333,8 +336,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(wsm + s * kPackedStageBytes, &tmap_w, j * kSuperBytes, n0, B.w_full + 8 * s);
           ++wj;
           for (int kk = 0; kk < 4; ++kk) {
-            const int s2 = xk % nx;
-            if (!mbar_wait(B.x_empty + 8 * s2, ((xk / nx) & 1) ^ 1, abort_flag)) {
+            const int s2 = xslot;
+            if (!mbar_wait(B.x_empty + 8 * s2, xph ^ 1u, abort_flag)) {
               ok = false;
               break;
             }
@@ -342,6 +345,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(xs + s2 * x_tile_bytes, &tmap_x, (4 * j + kk) * kKStep, m0,
                         B.x_full + 8 * s2);
             ++xk;
+            if (++xslot == nx) {
+              xslot = 0;
+              xph ^= 1u;
+            }
           }
         }
       }
@@ -357,9 +364,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer
+      // This one thread paces the tensor pipe: its per-k-step work is kept to
+      // waits, MMAs and commits (ring slots and phases as running counters,
+      // the X descriptor advanced by adding a stage's address units).
       const uint32_t idesc = idesc_bf16(kTileRows, args.bn);
-      int xk = 0, iter = 0;
-      int a_use0 = 0, a_use1 = 0;  // completed uses of A stage 0 / 1
+      const uint64_t xdesc0 = sw128_desc(xs);
+      const uint32_t xdesc_step = x_tile_bytes >> 4;  // descriptor address field in 16 B
+      int iter = 0, xslot = 0;
+      uint32_t xph = 0;  // phase of the X slot's next fill
+      uint32_t aph = 0;  // bit p: phase of A stage p's next fill
       bool ok = true, any = false;
       for (int w = cta; w < args.tiles * args.splits && ok; w += ncta, ++iter) {
         const Item it = item_of(w, args.splits, wstages);
@@ -369,25 +382,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        for (int ks = 4 * it.j0; ks < 4 * it.j1; ++ks) {
-          const int p = ks & 1, s2 = xk % nx;
-          const int use = p ? a_use1 : a_use0;
-          if (!mbar_wait(B.a_full + 8 * p, use & 1, abort_flag) ||
-              !mbar_wait(B.x_full + 8 * s2, (xk / nx) & 1, abort_flag)) {
+        const uint32_t d_acc = tmem + acc_col(b);
+        const int ks0 = 4 * it.j0, ks1 = 4 * it.j1;
+        for (int ks = ks0; ks < ks1; ++ks) {
+          const int p = ks & 1;
+          if (!mbar_wait(B.a_full + 8 * p, (aph >> p) & 1u, abort_flag) ||
+              !mbar_wait(B.x_full + 8 * xslot, xph, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t bdesc = sw128_desc(xs + s2 * x_tile_bytes);
+          const uint64_t bdesc =
+              xdesc0 + static_cast<uint64_t>(static_cast<uint32_t>(xslot) * xdesc_step);
+          const uint32_t a_t = tmem + a_col(p);
 #pragma unroll
           for (int kk = 0; kk < kKStep / 16; ++kk)
-            umma_ts_bf16(tmem + acc_col(b), tmem + a_col(p) + 8 * kk, bdesc + 2 * kk, idesc,
-                         (ks != 4 * it.j0 || kk != 0) ? 1u : 0u);
+            umma_ts_bf16(d_acc, a_t + 8 * kk, bdesc + 2 * kk, idesc,
+                         (ks != ks0 || kk != 0) ? 1u : 0u);
           any = true;
-          umma_commit(B.x_empty + 8 * s2);
+          umma_commit(B.x_empty + 8 * xslot);
           umma_commit(B.a_empty + 8 * p);
-          if (p) ++a_use1; else ++a_use0;
-          ++xk;
+          aph ^= 1u << p;
+          if (++xslot == nx) {
+            xslot = 0;
+            xph ^= 1u;
+          }
         }
         if (ok) umma_commit(B.acc_full + 8 * b);
       }
