@@ -262,7 +262,7 @@ int64_t q4_linear_crossover_m(int64_t n, int64_t k) {
     int64_t n, k, m;
   };
   static const Entry kTable[] = {
-      {4096, 3072, 4}, {1024, 3072, 6}, {3072, 4096, 4}, {9216, 3072, 6}, {3072, 9216, 4},
+      {4096, 3072, 4}, {1024, 3072, 6}, {3072, 4096, 4}, {9216, 3072, 4}, {3072, 9216, 4},
       {3840, 1280, 8}, {1280, 1280, 6}, {5120, 1280, 8}, {1280, 5120, 6},
   };
   // exact shape, else the entry nearest in weight count (log scale)

@@ -660,12 +660,14 @@ GemmPlan gemm_plan(int64_t n, int64_t k, int64_t m) {
   }
   // Too few tiles for the SMs (small M): split K, in 256-weight stages, so that
   // tiles x splits fill about one wave; partial tiles are added in the epilogue.
-  // The split costs a fixed ~9-10 us (partials out, counter, the last split's
-  // reduction and the clearing of the workspace, none of it overlapped), about
-  // the time of 24 of the CTA's 64-wide k-steps: split only when it removes
-  // more k-steps than that from every CTA (on B300: 1280 x 1280 at M = 375
+  // The split is not free: partials out, a counter, the last split's
+  // reduction and the clearing of the workspace, none of it overlapped.  For
+  // 64-token tiles that costs ~9-10 us, the time of ~24 of the CTA's 64-wide
+  // k-steps, and it grows with the tile width: split only when it removes more
+  // than 24 * BN / 64 k-steps from every CTA (on B300: 1280 x 1280 at M = 375
   // runs in 13.9 us whole and 19.5 us split in two; 1280 x 5120 in 39.3 us
-  // whole and 31.6 us split in two).
+  // whole and 31.6 us split in two; at M = 8, 32-token tiles, 1280 x 1280 split
+  // in five and 9216 x 3072 in two are faster than whole).
   p.splits = 1;
   const int64_t tiles = p.n_tiles * p.m_tiles, wstages = k / 256;
   if (tiles * 2 <= g) {
@@ -673,7 +675,7 @@ GemmPlan gemm_plan(int64_t n, int64_t k, int64_t m) {
     if (sp > wstages) sp = wstages;
     if (sp > 16) sp = 16;
     const int64_t ksteps = k / kKStep;
-    if (sp > 1 && ksteps * (sp - 1) > 24 * sp) p.splits = sp;
+    if (sp > 1 && ksteps * (sp - 1) * 64 > 24 * p.block_n * sp) p.splits = sp;
   }
   p.ws_bytes = 0;
   if (p.splits > 1) {

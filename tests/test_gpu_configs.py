@@ -371,7 +371,7 @@ def test_config5_crossover_shapes(torch, q4, oracle_mod, m):
 
 
 # the measured crossover table of q4_linear (largest M sent to the fp32 GEMV)
-CROSSOVER = {(4096, 3072): 4, (1024, 3072): 6, (3072, 4096): 4, (9216, 3072): 6,
+CROSSOVER = {(4096, 3072): 4, (1024, 3072): 6, (3072, 4096): 4, (9216, 3072): 4,
              (3072, 9216): 4, (3840, 1280): 8, (1280, 1280): 6, (5120, 1280): 8,
              (1280, 5120): 6}
 
