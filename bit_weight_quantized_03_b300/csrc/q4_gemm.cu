@@ -11,8 +11,8 @@
 // picked per shape so that the tiles fill the SMs in whole waves):
 //   warp 0     TMA producer: packed Q4 rows (2-D map over the bytes, box
 //              144 B x 128 rows = 256 weights per row) and bf16 X tiles (box
-//              64 x BN, 128-byte swizzle), each into a ring of mbarrier-guarded
-//              shared-memory stages.
+//              64 x BN, 128-byte swizzle, two per barrier), each into a ring of
+//              mbarrier-guarded shared-memory stages.
 //   warp 1     allocates all 512 TMEM columns and issues tcgen05.mma
 //              (kind::f16: A = the dequantized weights, read from TMEM; B = the
 //              X tile, read from shared memory; fp32 accumulator in TMEM) from
@@ -252,6 +252,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
   const int nx = args.x_stages;
+  // X tiles move in pairs (two 64-wide k-steps, one full and one empty
+  // barrier per pair): the MMA thread waits for X and releases it once per two
+  // k-steps.
+  const int nxp = nx / 2;
   const uint32_t x_tile_bytes = static_cast<uint32_t>(args.bn) * 128u;
   const uint32_t xs = base;                                    // X ring
   const uint32_t wsm = xs + static_cast<uint32_t>(nx) * x_tile_bytes;  // packed W ring
@@ -335,17 +339,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(B.w_full + 8 * s, kPackedStageBytes);
           tma_load_2d(wsm + s * kPackedStageBytes, &tmap_w, j * kSuperBytes, n0, B.w_full + 8 * s);
           ++wj;
-          for (int kk = 0; kk < 4; ++kk) {
-            const int s2 = xslot;
-            if (!mbar_wait(B.x_empty + 8 * s2, xph ^ 1u, abort_flag)) {
+          for (int pp = 0; pp < 2; ++pp) {
+            if (!mbar_wait(B.x_empty + 8 * xslot, xph ^ 1u, abort_flag)) {
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(B.x_full + 8 * s2, x_tile_bytes);
-            tma_load_2d(xs + s2 * x_tile_bytes, &tmap_x, (4 * j + kk) * kKStep, m0,
-                        B.x_full + 8 * s2);
-            ++xk;
-            if (++xslot == nx) {
+            mbar_arrive_expect_tx(B.x_full + 8 * xslot, 2 * x_tile_bytes);
+            const uint32_t dst = xs + static_cast<uint32_t>(xslot) * 2u * x_tile_bytes;
+            tma_load_2d(dst, &tmap_x, (4 * j + 2 * pp) * kKStep, m0, B.x_full + 8 * xslot);
+            tma_load_2d(dst + x_tile_bytes, &tmap_x, (4 * j + 2 * pp + 1) * kKStep, m0,
+                        B.x_full + 8 * xslot);
+            xk += 2;
+            if (++xslot == nxp) {
               xslot = 0;
               xph ^= 1u;
             }
@@ -357,8 +362,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // let the copies still in flight land before the CTA can exit
         for (int i = wj - kStagesW > 0 ? wj - kStagesW : 0; i < wj; ++i)
           mbar_wait(B.w_full + 8 * (i % kStagesW), (i / kStagesW) & 1);
-        for (int i = xk - nx > 0 ? xk - nx : 0; i < xk; ++i)
-          mbar_wait(B.x_full + 8 * (i % nx), (i / nx) & 1);
+        for (int i = xk / 2 - nxp > 0 ? xk / 2 - nxp : 0; i < xk / 2; ++i)
+          mbar_wait(B.x_full + 8 * (i % nxp), (i / nxp) & 1);
       }
     }
   } else if (warp == 1) {
@@ -366,7 +371,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---------------- MMA issuer
       // This one thread paces the tensor pipe: its per-k-step work is kept to
       // waits, MMAs and commits (ring slots and phases as running counters,
-      // the X descriptor advanced by adding a stage's address units).
+      // the X descriptor advanced by adding a stage's address units), and the
+      // loop takes the two k-steps of an X pair (A stages 0 and 1) together.
       const uint32_t idesc = idesc_bf16(kTileRows, args.bn);
       const uint64_t xdesc0 = sw128_desc(xs);
       const uint32_t xdesc_step = x_tile_bytes >> 4;  // descriptor address field in 16 B
@@ -384,26 +390,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t d_acc = tmem + acc_col(b);
         const int ks0 = 4 * it.j0, ks1 = 4 * it.j1;
-        for (int ks = ks0; ks < ks1; ++ks) {
-          const int p = ks & 1;
-          if (!mbar_wait(B.a_full + 8 * p, (aph >> p) & 1u, abort_flag) ||
+        for (int ks = ks0; ks < ks1; ks += 2) {
+          if (!mbar_wait(B.a_full, aph & 1u, abort_flag) ||
               !mbar_wait(B.x_full + 8 * xslot, xph, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint64_t bdesc =
-              xdesc0 + static_cast<uint64_t>(static_cast<uint32_t>(xslot) * xdesc_step);
-          const uint32_t a_t = tmem + a_col(p);
+              xdesc0 + static_cast<uint64_t>(static_cast<uint32_t>(xslot) * 2u * xdesc_step);
 #pragma unroll
           for (int kk = 0; kk < kKStep / 16; ++kk)
-            umma_ts_bf16(d_acc, a_t + 8 * kk, bdesc + 2 * kk, idesc,
+            umma_ts_bf16(d_acc, tmem + a_col(0) + 8 * kk, bdesc + 2 * kk, idesc,
                          (ks != ks0 || kk != 0) ? 1u : 0u);
           any = true;
+          umma_commit(B.a_empty);
+          if (!mbar_wait(B.a_full + 8, (aph >> 1) & 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kKStep / 16; ++kk)
+            umma_ts_bf16(d_acc, tmem + a_col(1) + 8 * kk, bdesc + xdesc_step + 2 * kk, idesc, 1u);
           umma_commit(B.x_empty + 8 * xslot);
-          umma_commit(B.a_empty + 8 * p);
-          aph ^= 1u << p;
-          if (++xslot == nx) {
+          umma_commit(B.a_empty + 8);
+          aph ^= 3u;
+          if (++xslot == nxp) {
             xslot = 0;
             xph ^= 1u;
           }
@@ -629,10 +642,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------ host side
 
+// X ring depth in 64-wide tiles: an even number (the tiles move in pairs), at
+// least 6 for every BN <= 224.
 int x_stages_for(int bn) {
   const int avail = kSmemBudget - 1024 /* alignment */ - kStagesW * kPackedStageBytes - kBarBytes;
   int s = avail / (bn * 128);
-  return s > kMaxXStages ? kMaxXStages : s;
+  s = s > kMaxXStages ? kMaxXStages : s;
+  return s & ~1;
 }
 
 }  // namespace
