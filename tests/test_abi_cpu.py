@@ -204,6 +204,34 @@ def test_workspace_sizes_are_consistent(q4):
     assert L.q4_linear_crossover_m(4096, 288) == q4.GEMV_MAX_M
 
 
+def _gemm_split_ws(n, m, splits, bn_tiles):
+    """Workspace of a q4_gemm that splits K: the per-tile arrival counters
+    (rounded up to 256 bytes), then splits x m x n fp32 partials."""
+    return (bn_tiles * 4 + 255) // 256 * 256 + splits * m * n * 4
+
+
+@pytest.mark.parametrize("n,k,m,expect", [
+    # K = 1280 at M = 375 (64-token tiles): a 2-way split would remove only 10
+    # k-steps per CTA, less than its fixed cost -> whole tiles, no workspace
+    (1280, 1280, 375, 0),
+    (3840, 1280, 375, 0),
+    # K = 5120 at M = 375: the 2-way split removes 40 k-steps -> split
+    (1280, 5120, 375, _gemm_split_ws(1280, 375, 2, 10 * 6)),
+    # small M (32-token tiles): the splits that pay stay
+    (4096, 3072, 8, _gemm_split_ws(4096, 8, 4, 32)),
+    (1280, 1280, 8, _gemm_split_ws(1280, 8, 5, 10)),
+    (9216, 3072, 8, _gemm_split_ws(9216, 8, 2, 72)),
+    # large M: one wave or more of whole tiles
+    (3840, 1280, 3000, 0),
+    (1280, 5120, 3000, 0),
+])
+def test_gemm_split_k_plan(q4, n, k, m, expect):
+    """The GEMM planner splits K only when that removes more than 24 * BN / 64
+    of a CTA's 64-wide k-steps (148 SMs assumed without a GPU); the workspace
+    query shows the decision."""
+    assert q4.lib().q4_gemm_workspace_bytes(n, k, m) == expect
+
+
 def test_gemv_workspace_covers_every_launch_of_a_batched_call(q4):
     """A q4_gemv call with m >= 2 rows (k % 256 == 0) runs launches of up to 4
     rows of the batched tile kernel (8 warps per SM) and, for a single leftover
