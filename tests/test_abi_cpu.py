@@ -232,6 +232,30 @@ def test_gemm_split_k_plan(q4, n, k, m, expect):
     assert q4.lib().q4_gemm_workspace_bytes(n, k, m) == expect
 
 
+# q4_linear's measured table: the largest M sent to the fp32 GEMV per shape
+CROSSOVER_TABLE = {(4096, 3072): 4, (1024, 3072): 6, (3072, 4096): 4, (9216, 3072): 4,
+                   (3072, 9216): 4, (3840, 1280): 8, (1280, 1280): 6, (5120, 1280): 8,
+                   (1280, 5120): 6}
+
+
+def test_linear_crossover_table_and_nearest_shape(q4):
+    """Each measured shape returns its entry; another shape takes the entry
+    whose weight count is nearest on a log scale; k % 256 != 0 has no
+    tensor-core path and returns the GEMV's limit."""
+    L = q4.lib()
+    for (n, k), m in CROSSOVER_TABLE.items():
+        assert L.q4_linear_crossover_m(n, k) == m, (n, k)
+    import math
+
+    def nearest(n, k):
+        return min(CROSSOVER_TABLE.items(),
+                   key=lambda e: abs(math.log(n * k / (e[0][0] * e[0][1]))))[1]
+    for n, k in [(4096, 2048), (2048, 1280), (100, 256), (131072, 3072), (7000, 5120)]:
+        assert L.q4_linear_crossover_m(n, k) == nearest(n, k), (n, k)
+    assert L.q4_linear_crossover_m(4096, 3104) == q4.GEMV_MAX_M
+    assert L.q4_linear_crossover_m(0, 3072) == q4.GEMV_MAX_M
+
+
 def test_gemv_workspace_covers_every_launch_of_a_batched_call(q4):
     """A q4_gemv call with m >= 2 rows (k % 256 == 0) runs launches of up to 4
     rows of the batched tile kernel (8 warps per SM) and, for a single leftover
