@@ -301,9 +301,9 @@ def run_ours(args):
 # traffic grows with the layer count).  Each entry is used only while the
 # kernel sources hash to what they were when captured, else it is null.
 STEP_TRAFFIC = {
-    "per_launch": {"bytes_per_step": 26 * 65_985_280,
+    "per_launch": {"bytes_per_step": 13 * 133_615_616,
                    "sources": ("q4_gemv_b1.cu", "q4_gemv_tile.cuh"),
-                   "sha16": "2818c95998691340"},
+                   "sha16": "356d83a8628bbfcf"},
     "fused": {"bytes_per_step": 13 * 135_205_376,
               "sources": ("q4_chain.cu", "q4r_tile.cuh"),
               "sha16": "5e9eade3da070177"},
@@ -526,7 +526,8 @@ def _run_single_gemv(args, dev, stream, hbm, torch):
 PATH_NOTES = {
     "fused": "one q4_chain launch per step on the repacked weights",
     "chain": "one q4_gemv_chain launch per step on the GGUF weights",
-    "per_launch": "104 q4_gemv launches per step with programmatic dependent launch",
+    "per_launch": ("104 q4_gemv_prefetch launches per step with programmatic dependent launch, "
+                   "each prefetching the next product's weights into L2"),
 }
 STEP_FUNCTION = {
     "fused": "per layer: qkv = Wqkv x; h = x + Wo q; g = W1h sigmoid(W1h) W3h; x' = h + W2 g",

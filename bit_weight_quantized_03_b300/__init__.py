@@ -22,7 +22,7 @@ from ._lib import (BF16, BLOCK_BYTES, CHAIN_MAX_LINKS, CHAIN_MAX_STAGES, GemvSta
                    OP_SWIGLU, Q4Error, REPACK_TILE_BYTES, check, lib, status_string)
 
 __all__ = [
-    "q4_quantize", "q4_dequant_rows", "q4_gemv", "q4_gemv_noalloc", "q4_gemv_chain", "q4_gemm", "q4_embed_gather", "q4_linear",
+    "q4_quantize", "q4_dequant_rows", "q4_gemv", "q4_gemv_prefetch", "q4_gemv_noalloc", "q4_gemv_chain", "q4_gemm", "q4_embed_gather", "q4_linear",
     "q4_gemv_workspace_bytes", "q4_gemm_workspace_bytes", "q4_linear_workspace_bytes",
     "q4_linear_crossover_m", "Workspace", "Q4Error", "lib", "packed_bytes",
     "q4_repack", "q4_repack_bytes", "q4_chain", "q4_chain_workspace_bytes", "q4_gemv_r",
@@ -156,6 +156,24 @@ def q4_gemv(W, n: int, k: int, x, y=None, workspace=None, status=None, flags: in
     buf, nbytes = _workspace(workspace, q4_gemv_workspace_bytes(n, k, m))
     check(lib().q4_gemv(_ptr(W), n, k, _ptr(x), m, ldx, _ptr(y), ldy, _ptr(buf), nbytes,
                         _ptr(status), flags, _stream(stream)), "q4_gemv")
+    return y
+
+
+def q4_gemv_prefetch(W, n: int, k: int, x, prefetch=None, y=None, workspace=None, status=None,
+                     flags: int = 0, stream=None):
+    """q4_gemv that prefetches the tensor `prefetch` (e.g. the next product's
+    weights; contiguous, its byte size a multiple of 16) into L2 while it runs."""
+    torch = _torch()
+    m = x.shape[0]
+    ldx = _row_stride(x, "x")
+    if y is None:
+        y = torch.empty((m, n), dtype=torch.float32, device=x.device)
+    ldy = _row_stride(y, "y")
+    pbytes = 0 if prefetch is None else prefetch.numel() * prefetch.element_size()
+    buf, nbytes = _workspace(workspace, q4_gemv_workspace_bytes(n, k, m))
+    check(lib().q4_gemv_prefetch(_ptr(W), n, k, _ptr(x), m, ldx, _ptr(y), ldy, _ptr(buf), nbytes,
+                                 _ptr(status), flags, _ptr(prefetch), pbytes, _stream(stream)),
+          "q4_gemv_prefetch")
     return y
 
 

@@ -64,6 +64,8 @@ SIGNATURES = {
     "q4_dequant_rows": (_st, [_vp, _i64, _i64, _i64, _vp, ctypes.c_int, _vp]),
     "q4_gemv": (_st, [_vp, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _vp, _sz, _vp, _u32, _vp]),
     "q4_gemv_workspace_bytes": (_sz, [_i64, _i64, _i64]),
+    "q4_gemv_prefetch": (_st, [_vp, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _vp, _sz, _vp, _u32,
+                               _vp, _sz, _vp]),
     "q4_gemv_noalloc": (_st, [_vp, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _vp, _u32, _vp]),
     "q4_gemv_q8": (_st, [_vp, _i64, _i64, _vp, _vp, _vp]),
     "q4_gemv_chain": (_st, [ctypes.POINTER(GemvStage), ctypes.c_int32, _vp, _sz, _vp, _u32, _vp]),

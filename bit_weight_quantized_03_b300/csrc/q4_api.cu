@@ -132,6 +132,24 @@ q4_status q4_gemv(const void* W, int64_t n, int64_t k, const float* x, int64_t m
                                    workspace, status_dev, flags, reinterpret_cast<cudaStream_t>(s)));
 }
 
+q4_status q4_gemv_prefetch(const void* W, int64_t n, int64_t k, const float* x, int64_t m,
+                           int64_t ldx, float* y, int64_t ldy, void* workspace, size_t ws_bytes,
+                           int32_t* status_dev, uint32_t flags, const void* prefetch,
+                           size_t prefetch_bytes, q4_stream_t s) {
+  q4_status st = q4::gemv_check_args(W, n, k, x, m, ldx, y, ldy);
+  if (st != Q4_OK) return st;
+  if (prefetch_bytes != 0 && prefetch == nullptr) return Q4_ERR_INVALID_ARG;
+  if (prefetch_bytes != 0 && (!aligned(prefetch, 16) || prefetch_bytes % 16 != 0))
+    return Q4_ERR_MISALIGNED;
+  const q4::GemvPlan plan = q4::gemv_plan(n, k, m);
+  if (plan.ws_bytes > 0 && (workspace == nullptr || ws_bytes < plan.ws_bytes))
+    return Q4_ERR_WORKSPACE;
+  if (plan.ws_bytes > 0 && !aligned(workspace, 16)) return Q4_ERR_MISALIGNED;
+  return from_cuda(q4::gemv_launch(plan, static_cast<const uint8_t*>(W), n, k, x, m, ldx, y, ldy,
+                                   workspace, status_dev, flags, reinterpret_cast<cudaStream_t>(s),
+                                   prefetch, prefetch_bytes));
+}
+
 size_t q4_gemm_workspace_bytes(int64_t n, int64_t k, int64_t m) {
   if (n <= 0 || k <= 0 || k % 256 || m <= 0) return 0;
   return q4::gemm_plan(n, k, m).ws_bytes;

@@ -451,13 +451,14 @@ GemvPlan gemv_plan(int64_t n, int64_t k, int64_t m) {
 
 cudaError_t gemv_launch(const GemvPlan& plan, const uint8_t* W, int64_t n, int64_t k,
                         const float* x, int64_t m, int64_t ldx, float* y, int64_t ldy,
-                        void* workspace, int32_t* status, uint32_t flags, cudaStream_t s) {
+                        void* workspace, int32_t* status, uint32_t flags, cudaStream_t s,
+                        const void* pf, uint64_t pf_bytes) {
   const bool pdl = (flags & 1u) != 0;
   if (plan.fast && plan.b1 && m == 1) {
     const size_t cnt_bytes = (static_cast<size_t>(plan.groups) * 4 + 255) / 256 * 256;
     return gemv_b1_launch(W, n, k, x, y, static_cast<int32_t*>(workspace),
                           reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + cnt_bytes),
-                          plan.units, plan.warps, status, flags, s);
+                          plan.units, plan.warps, status, flags, s, pf, pf_bytes);
   }
   if (plan.fast && plan.bm && m >= 2) {
     // Launches of up to kMaxBatchRows rows (fewer where x would not fit in

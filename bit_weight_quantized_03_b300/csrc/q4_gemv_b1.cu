@@ -83,6 +83,8 @@ struct B1Params {
   int64_t units, warps;
   int32_t* status;
   uint32_t flags;
+  const uint8_t* pf;   // region prefetched into L2 (the next product's weights), or null
+  uint64_t pf_bytes;   // a multiple of 16
 };
 
 // A partial row sum as one 64-bit word: the float's bits below a presence tag.
@@ -168,6 +170,19 @@ __device__ __forceinline__ void gemv_tile_body(const CUtensorMap& tmap, const B1
     if (++islot == kStages) islot = 0;
   };
   pdl_allow_dependents();
+  // L2 prefetch of the region handed in (in a decode step, the weights of the
+  // product after this one), split over the CTAs in 32 KB bulk prefetches: it
+  // keeps HBM busy through this product's hand-offs.
+  if (p.pf_bytes != 0 && threadIdx.x == 0) {
+    const uint64_t share = ((p.pf_bytes + gridDim.x - 1) / gridDim.x + 15) / 16 * 16;
+    const uint64_t lo = share * blockIdx.x;
+    const uint64_t hi = lo + share < p.pf_bytes ? lo + share : p.pf_bytes;
+    for (uint64_t o = lo; o < hi; o += 32768) {
+      const uint32_t sz = static_cast<uint32_t>(hi - o < 32768 ? hi - o : 32768);
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.pf + o), "r"(sz)
+                   : "memory");
+    }
+  }
   // The weights never depend on the previous kernel: in the chain shape the
   // ring is filled while that kernel still runs.
   if (kEarlyRing)
@@ -450,7 +465,8 @@ bool gemv_b1_supports(int64_t k) { return b1_smem_bytes(k, kSoloWarps) <= kSoloM
 
 cudaError_t gemv_b1_launch(const uint8_t* W, int64_t n, int64_t k, const float* x, float* y,
                            int32_t* counters, float* partials, int64_t units, int64_t warps,
-                           int32_t* status, uint32_t flags, cudaStream_t s) {
+                           int32_t* status, uint32_t flags, cudaStream_t s, const void* pf,
+                           uint64_t pf_bytes) {
   const int64_t rowbytes = k / 32 * kBlockBytes;
   CUtensorMap tmap;
   if (!make_tmap(&tmap, W, n, k)) return cudaErrorInvalidValue;
@@ -468,6 +484,8 @@ cudaError_t gemv_b1_launch(const uint8_t* W, int64_t n, int64_t k, const float* 
   p.units = units;
   p.status = status;
   p.flags = flags;
+  p.pf = static_cast<const uint8_t*>(pf);
+  p.pf_bytes = pf_bytes;
   const size_t pair_smem = b1_smem_bytes(k, kPairWarps);
   // The chain shape pays while the next product's ring fill is a real share of
   // that product: for the 7-32 MB decoder products it takes ~13 % off a decode
@@ -516,6 +534,8 @@ cudaError_t gemv_bm_launch(const uint8_t* W, int64_t n, int64_t k, const float* 
   p.warps = gemv_bm_warps(units);
   p.status = status;
   p.flags = flags;
+  p.pf = nullptr;
+  p.pf_bytes = 0;
   const size_t smem = b1_smem_bytes(k, kPairWarps, static_cast<int>(mb));
   switch (mb) {
     case 2: return pdl ? launch_batched<2, true>(tmap, p, smem, pdl, s)

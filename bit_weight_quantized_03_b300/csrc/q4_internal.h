@@ -45,9 +45,12 @@ struct GemvPlan {
   size_t ws_bytes;    // workspace the plan needs
 };
 GemvPlan gemv_plan(int64_t n, int64_t k, int64_t m);
+// pf, pf_bytes: a region (16-byte aligned, a multiple of 16 bytes) to prefetch
+// into L2 while the product runs; taken by the batch-1 path, ignored elsewhere.
 cudaError_t gemv_launch(const GemvPlan& plan, const uint8_t* W, int64_t n, int64_t k,
                         const float* x, int64_t m, int64_t ldx, float* y, int64_t ldy,
-                        void* workspace, int32_t* status, uint32_t flags, cudaStream_t s);
+                        void* workspace, int32_t* status, uint32_t flags, cudaStream_t s,
+                        const void* pf = nullptr, uint64_t pf_bytes = 0);
 
 // Rows of x one batched tile launch carries (q4_gemv_b1.cu).
 constexpr int64_t kMaxBatchRows = 4;
@@ -62,7 +65,8 @@ cudaError_t gemv_bm_launch(const uint8_t* W, int64_t n, int64_t k, const float* 
 bool gemv_b1_supports(int64_t k);
 cudaError_t gemv_b1_launch(const uint8_t* W, int64_t n, int64_t k, const float* x, float* y,
                            int32_t* counters, float* partials, int64_t units, int64_t warps,
-                           int32_t* status, uint32_t flags, cudaStream_t s);
+                           int32_t* status, uint32_t flags, cudaStream_t s,
+                           const void* pf = nullptr, uint64_t pf_bytes = 0);
 
 // --------------------------------------------------------------- GEMV chain
 constexpr int kMaxChain = 128;      // links per launch

@@ -19,8 +19,9 @@ input -- Wqkv = [wq; wk; wv] (6144 x 3072), W13 = [w1; w3] (18432 x 3072) --
 plus wo (3072 x 4096) and w2 (3072 x 9216), each a contiguous run of Q4_0 rows.
 A decode step is 4 dependent products per layer (104 per step), run either as
 one q4_gemv_chain launch (persistent, the weight stream never stops between
-products) or as 104 q4_gemv launches with programmatic dependent launch
-between them; either is captured in a CUDA graph.
+products) or as 104 q4_gemv_prefetch launches with programmatic dependent
+launch between them, each prefetching the next product's weights into L2;
+either is captured in a CUDA graph.
 """
 from __future__ import annotations
 
@@ -28,7 +29,7 @@ import synth
 
 from . import (FLAG_PDL, OP_RESIDUAL, OP_SWIGLU, Link, LinkOut, Workspace,
                interleave_gate_rows, q4_chain, q4_chain_workspace_bytes, q4_gemm, q4_gemv,
-               q4_gemv_chain, q4_quantize, q4_repack)
+               q4_gemv_chain, q4_gemv_prefetch, q4_quantize, q4_repack)
 
 
 def _quantize_rows(parts, k, device, torch):
@@ -112,15 +113,18 @@ class DecoderStack:
         return 4 * self.layers
 
     def _layer(self, l, x_in, stream):
+        # each product prefetches the next one's weights into L2 (the last of
+        # the step those of the next step's first product)
         W, (nq, h), = self.W[l], self.shapes["qkv"]
-        q4_gemv(W["qkv"], nq, h, x_in, y=self.y_qkv, workspace=self.ws, flags=FLAG_PDL,
-                stream=stream)
-        q4_gemv(W["wo"], h, self.QDIM, self.y_qkv[:, :self.QDIM], y=self.y_o, workspace=self.ws,
-                flags=FLAG_PDL, stream=stream)
-        q4_gemv(W["w13"], 2 * self.FFN, h, self.y_o, y=self.y_13, workspace=self.ws,
-                flags=FLAG_PDL, stream=stream)
-        q4_gemv(W["w2"], h, self.FFN, self.y_13[:, :self.FFN], y=self.x, workspace=self.ws,
-                flags=FLAG_PDL, stream=stream)
+        nxt = self.W[(l + 1) % self.layers]["qkv"]
+        q4_gemv_prefetch(W["qkv"], nq, h, x_in, prefetch=W["wo"], y=self.y_qkv, workspace=self.ws,
+                         flags=FLAG_PDL, stream=stream)
+        q4_gemv_prefetch(W["wo"], h, self.QDIM, self.y_qkv[:, :self.QDIM], prefetch=W["w13"],
+                         y=self.y_o, workspace=self.ws, flags=FLAG_PDL, stream=stream)
+        q4_gemv_prefetch(W["w13"], 2 * self.FFN, h, self.y_o, prefetch=W["w2"], y=self.y_13,
+                         workspace=self.ws, flags=FLAG_PDL, stream=stream)
+        q4_gemv_prefetch(W["w2"], h, self.FFN, self.y_13[:, :self.FFN], prefetch=nxt, y=self.x,
+                         workspace=self.ws, flags=FLAG_PDL, stream=stream)
 
     def step_only(self, key, stream=None):
         """The products of one kind ("qkv", "wo", "w13" or "w2") of a decode step,
@@ -202,7 +206,8 @@ class DecoderStack:
     def step(self, x_in, stream=None, chain: bool = False):
         """One decode step on the device: x_in [1, 3072] fp32 -> self.x [1, 3072].
         chain=True runs the 104 products as one q4_gemv_chain launch; otherwise
-        one q4_gemv launch each (programmatic dependent launch between them)."""
+        one q4_gemv_prefetch launch each (programmatic dependent launch between
+        them, each prefetching the next product's weights into L2)."""
         if chain:
             q4_gemv_chain(self.links(x_in), workspace=self.chain_ws, stream=stream)
             return self.x

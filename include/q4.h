@@ -125,6 +125,26 @@ q4_status q4_gemv(const void* W, int64_t n, int64_t k, const float* x, int64_t m
                   uint32_t flags, q4_stream_t s);
 size_t q4_gemv_workspace_bytes(int64_t n, int64_t k, int64_t m);
 
+/* q4_gemv that also prefetches a region of device memory into L2 while it
+ * runs: in a decode step, the weights of the next product.  Each product of
+ * the step waits on the one before it (programmatic dependent launch), and
+ * the part of a product's weights that its early ring fill does not cover
+ * would otherwise stream from HBM only after that wait; prefetched, it comes
+ * from L2 while HBM works through the hand-offs.  The arithmetic and the
+ * result are exactly q4_gemv's.  The pages do not describe this; it is
+ * scheduling only.
+ *   prefetch        the region (16-byte aligned), read-only, never written by
+ *                   the call; NULL with prefetch_bytes == 0 is plain q4_gemv.
+ *   prefetch_bytes  a multiple of 16 (a Q4 matrix with k % 256 == 0 is).
+ * Taken by the batch-1 path (m == 1, k % 256 == 0); ignored otherwise.  The
+ * region should not be written by the kernel before this one on the stream
+ * when Q4_FLAG_PDL is set (it is read as W is: early).  Other arguments,
+ * errors and the workspace as for q4_gemv. */
+q4_status q4_gemv_prefetch(const void* W, int64_t n, int64_t k, const float* x, int64_t m,
+                           int64_t ldx, float* y, int64_t ldy, void* workspace, size_t ws_bytes,
+                           int32_t* status_dev, uint32_t flags, const void* prefetch,
+                           size_t prefetch_bytes, q4_stream_t s);
+
 /* q4_gemv for callers that cannot allocate device memory (a host that embeds
  * the library in a fixed memory pool where cudaMalloc is forbidden, a
  * real-time loop that must not allocate once streaming has started, a plugin

@@ -140,6 +140,22 @@ def _bad_link(q4, **kw):
     return arr
 
 
+def test_gemv_prefetch_host_validation(q4):
+    """The prefetch region of q4_gemv_prefetch is checked before anything is
+    launched: NULL with a size, a pointer off 16 bytes or a size off a multiple
+    of 16 is refused; the other arguments are q4_gemv's."""
+    L = q4.lib()
+    W, X, Y, P = (i << 20 for i in (1, 2, 3, 4))  # 16-byte aligned fake device addresses
+    args = (W, 8, 256, X, 1, 256, Y, 8, None, 0, None, 0)
+    assert L.q4_gemv_prefetch(*args, None, 16, None) == q4.ERR_INVALID_ARG
+    assert L.q4_gemv_prefetch(*args, P + 8, 16, None) == q4.ERR_MISALIGNED
+    assert L.q4_gemv_prefetch(*args, P, 24, None) == q4.ERR_MISALIGNED
+    # a good region gets as far as q4_gemv's own checks (no workspace here)
+    assert L.q4_gemv_prefetch(*args, P, 32, None) == q4.ERR_WORKSPACE
+    assert L.q4_gemv_prefetch(W, 8, 48, X, 1, 48, Y, 8, None, 0, None, 0, P, 16,
+                              None) == q4.ERR_UNSUPPORTED_SHAPE
+
+
 def test_gemv_q8_host_validation(q4):
     L = q4.lib()
     A16 = 1 << 20  # a 16-byte-aligned fake address: nothing is launched on these paths

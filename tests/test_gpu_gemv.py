@@ -179,3 +179,22 @@ def test_gemv_workspace_shared_across_shapes(torch, q4, oracle_mod):
         assert ok, (n, k, m, info)
         torch.cuda.synchronize()
         assert int(ws.buf.count_nonzero().item()) == 0
+
+
+@pytest.mark.parametrize("pdl", [False, True])
+def test_gemv_prefetch_gives_q4_gemv_result(torch, q4, oracle_mod, pdl):
+    """q4_gemv_prefetch is q4_gemv plus an L2 prefetch of another region: the
+    result is q4_gemv's bit for bit (and within the oracle's bound), whether
+    the region is another matrix, the call's own W or absent."""
+    n, k = 4096, 3072
+    W, x = _case(oracle_mod, n, k, 1, seed=77)
+    W2, _ = _case(oracle_mod, 3072, 4096, 1, seed=78)
+    Wd, xd, W2d = (torch.from_numpy(a).cuda() for a in (W, x, W2))
+    flags = q4.FLAG_PDL if pdl else 0
+    ref = q4.q4_gemv(Wd, n, k, xd, flags=flags).cpu().numpy()
+    Y, S = oracle_mod.matmul(W, n, k, x)
+    for region in (W2d, Wd, None):
+        got = q4.q4_gemv_prefetch(Wd, n, k, xd, prefetch=region, flags=flags).cpu().numpy()
+        assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+        ok, info = within_tol(got, Y, S, TOL)
+        assert ok, info
